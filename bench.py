@@ -1,0 +1,417 @@
+"""Benchmark of the fused attention forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step = one fa_fwd call over the whole workload (every (batch, head) and
+every query row): the complete hot path.  Default workload: B=2, H=32,
+N=8192, d=128, bf16 inputs drawn N(0,1)*0.5 from a seed (the compute-bound
+headline shape).  The metric is attention-forward TFLOP/s counting
+4*B*H*N^2*d flops per step.
+
+`value` is device-timed (CUDA events on the launching stream around exactly K
+steps, inputs resident in HBM; 268 MB of inputs+outputs per step exceed the
+129 MB L2).  `e2e` is the same metric with each step's host->device copies of
+Q, K, V (pinned memory) and the device->host copies of O and lse inside the
+timed region.  `roofline` compares the kernel with the measured dense bf16
+tensor peak.  `cpu_baseline` times the fp64 CPU oracle on a bounded sample of
+the same workload on the host cores (rank 0 only).
+
+Multi-GPU (torchrun, one process per GPU): each rank runs its own independent
+copy of the workload (attention heads are independent; no collective on the
+data path): weak scaling, value = all ranks' flops / max-over-ranks time.
+
+`--impl reference` times the CPU oracle (the only reference implementation
+there is) on bounded samples of the workload and prints the same line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (4·B·H·N²·d) on 1 GB300 and % of dense tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_BF16_TFLOPS = 1900.0
+NOMINAL_TF32_OVER_BF16 = 0.5  # dense TF32 rate relative to dense bf16 (1.1 vs 2.25 PFLOP/s nominal)
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def reduce_max(value: float, dist, device=None) -> float:
+    """Maximum of a float over all ranks (identity without a process group)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, dist, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources: ties a stored ncu traffic figure to the
+    kernel it was measured on."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_tiled_attention_04_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        with open(path) as f:
+            lines = [ln.strip() for ln in f if ln.strip() and not ln.startswith("#")]
+    except OSError:
+        return None
+    want = kernel_source_hash()
+    for ln in lines:
+        kv = dict(x.split("=", 1) for x in ln.split() if "=" in x)
+        if kv.get("workload") == workload and kv.get("kernel_hash") == want:
+            try:
+                return float(kv["dram_bytes_per_launch"])
+            except (KeyError, ValueError):
+                return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+        return False
+
+    def summary(self, busy_threshold_frac: float = 0.0):
+        try:
+            with open(self.file.name) as f:
+                rows = [r.strip() for r in f if r.strip()]
+        finally:
+            try:
+                os.unlink(self.file.name)
+            except OSError:
+                pass
+        sm, smax, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names[1:], parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- CPU oracle
+def cpu_oracle_rate(w, q, k, v, target_s: float, max_rows: int | None = None):
+    """Time the fp64 oracle on seeded rows of the workload, sized to run
+    about `target_s` seconds on every host core.  Returns (TFLOP/s, cores,
+    rows, seconds)."""
+    import oracle
+    from exact_tiled_attention_04_gb300 import inputs as I
+    cores = oracle.default_threads()
+    rows = I.sample_rows(w, 64, seed_offset=1000)
+    t0 = time.perf_counter()
+    oracle.attention_f64(q, k, v, float(w.scale), rows=rows)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    n = int(64 * target_s / dt)
+    n = max(cores, min(n, max_rows or n, w.B * w.H * w.N))
+    rows = I.sample_rows(w, n, seed_offset=1001)
+    t0 = time.perf_counter()
+    oracle.attention_f64(q, k, v, float(w.scale), rows=rows)
+    dt = time.perf_counter() - t0
+    return oracle.flops(w.B, w.H, w.N, w.d, rows=n) / dt / 1e12, cores, n, dt
+
+
+# ------------------------------------------------------------------- arms
+def run_reference(args, w):
+    """The CPU oracle as the reference arm: each step is a bounded sample of
+    the workload's query rows."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from exact_tiled_attention_04_gb300 import inputs as I
+    q, k, v = I.make(w)
+    cores = oracle.default_threads()
+    budget_s = 150.0 / max(1, args.steps + args.warmup)
+    rows = I.sample_rows(w, 16, seed_offset=2000)
+    t0 = time.perf_counter()
+    oracle.attention_f64(q, k, v, float(w.scale), rows=rows)
+    per_row = max((time.perf_counter() - t0) / 16, 1e-7)
+    n = int(max(1, min(4096, w.B * w.H * w.N, budget_s / per_row)))
+    for i in range(args.warmup):
+        oracle.attention_f64(q, k, v, float(w.scale), rows=I.sample_rows(w, n, seed_offset=3000 + i))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.attention_f64(q, k, v, float(w.scale), rows=I.sample_rows(w, n, seed_offset=4000 + i))
+    dt = time.perf_counter() - t0
+    value = oracle.flops(w.B, w.H, w.N, w.d, rows=n) * args.steps / dt / 1e12
+    sample = f"{n} seeded query rows of the workload per step (of {w.B * w.H * w.N}), fp64, {cores} threads"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": config_of(w, args.gpus),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, n_gpus: int):
+    nbytes = 4 * w.B * w.H * w.N * w.d * (2 if w.dtype == "bf16" else 4) + 4 * w.B * w.H * w.N
+    l2 = (f"inputs larger than L2: q,k,v,o,lse = {nbytes / 1e6:.0f} MB per step (L2 129 MB), no flush"
+          if nbytes > 129e6 else f"L2-resident: q,k,v,o,lse = {nbytes / 1e6:.1f} MB per step")
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype,
+            "inputs": f"seeded N(0,1) x {w.factor}", "scale": float(w.scale), "l2": l2,
+            "parallelism": f"independent replica per GPU x{n_gpus}"}
+
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+    from exact_tiled_attention_04_gb300 import binding as fab
+    from exact_tiled_attention_04_gb300 import inputs as I
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(world, "nccl")
+    fab.load()
+
+    # per-rank inputs (weak scaling: every rank its own seeded copy)
+    wr = I.Workload(w.name, w.B, w.H, w.N, w.d, w.dtype, w.seed + 17 * rank, w.factor,
+                    w.identical_k_heads, w.q_scaled_heads, w.oracle_rows, w.note)
+    q, k, v = I.make(wr)
+
+    def host_tensor(x):
+        if w.dtype == "bf16":
+            return torch.from_numpy(I.bf16_bits(x).view(np.int16)).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(x, np.float32))
+
+    hq, hk, hv = (host_tensor(x).pin_memory() for x in (q, k, v))
+    dq, dk, dv = (t.to(dev) for t in (hq, hk, hv))
+    do = torch.empty_like(dq)
+    dlse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+    dt_code = fab.FA_DTYPE_BF16 if w.dtype == "bf16" else fab.FA_DTYPE_F32
+    scale = float(w.scale)
+    launches = 0
+
+    def step():
+        nonlocal launches
+        st = fab.fa_fwd(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), do.data_ptr(), dlse.data_ptr(),
+                        w.B, w.H, w.N, w.d, scale, dt_code, sp)
+        if st != fab.FA_OK:
+            raise fab.FAError(st, "fa_fwd")
+        launches += 1
+
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    st = fab.fa_device_status(sp)
+    if st != fab.FA_OK:
+        raise fab.FAError(st, "warm-up")
+
+    # ---- device-timed region: exactly K steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches = 0
+    with ClockSampler(local) as clocks:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                step()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    timed_launches = launches
+    st = fab.fa_device_status(sp)
+    if st != fab.FA_OK:
+        raise fab.FAError(st, "timed region")
+    ms_local = ev0.elapsed_time(ev1)
+    ms_total = reduce_max(ms_local, dist, dev)
+    flops_rank = w.flops() * args.steps
+    flops_all = reduce_sum(flops_rank, dist, dev)
+    value = flops_all / (ms_total * 1e-3) / 1e12
+    kernel_ms = ms_local / args.steps  # one kernel per step on this stream
+    clk = clocks.summary()
+
+    # ---- end to end: host copies inside the timed region
+    e2e_steps = max(3, min(args.steps, 20))
+    ho = torch.empty_like(hq).pin_memory()
+    hl = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            step()
+            ho.copy_(do, non_blocking=True)
+            hl.copy_(dlse, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1), dist, dev)
+    e2e_value = reduce_sum(w.flops() * e2e_steps, dist, dev) / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peaks = measured_peaks()
+    bf16_peak = (peaks or {}).get("bf16_tflops")
+    peak_note = "measured bf16 burst (MEASURED_PEAKS.json)"
+    if not bf16_peak:
+        bf16_peak, peak_note = FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16"
+    peak = bf16_peak if w.dtype == "bf16" else bf16_peak * NOMINAL_TF32_OVER_BF16
+    if w.dtype != "bf16":
+        peak_note += " x nominal tf32/bf16 ratio 0.5"
+    achieved = w.flops() / (kernel_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                "frac": achieved / peak, "traffic": stored_traffic(w.name),
+                "kernel": f"fa_fwd_kernel<{'tf32' if w.dtype != 'bf16' else 'bf16'},{w.d}>",
+                "peak_source": peak_note,
+                "algorithmic_flops_per_launch": w.flops(),
+                "algorithmic_bytes_per_launch": 4 * w.B * w.H * w.N * w.d * (2 if w.dtype == "bf16" else 4)
+                + 4 * w.B * w.H * w.N}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": config_of(w, world),
+        "frac_of_peak": value / world / peak,
+        "roofline": roofline,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
+        "gpu_launches": timed_launches,
+        "clocks": {k2: clk[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        rate, cores, n, secs = cpu_oracle_rate(wr, q, k, v, target_s=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"{n} seeded query rows of the workload "
+                                          f"(of {w.B * w.H * w.N}), fp64 three-pass, {secs:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None, help="workload name (default: the headline shape)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    from exact_tiled_attention_04_gb300 import inputs as I
+    w = I.WORKLOADS[args.workload or I.HEADLINE]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

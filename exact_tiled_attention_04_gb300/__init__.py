@@ -2,4 +2,13 @@
 
 O = softmax(scale * Q K^T) V and the per-row log-sum-exp, computed by one
 fused CUDA kernel that never writes the N x N score matrix to HBM.
+
+The C ABI (include/fa.h) is mirrored one to one by ``binding``; ``inputs``
+draws the seeded synthetic workloads.  Importing the package loads no CUDA
+code; the first call into ``binding`` loads the library and fails loudly if it
+was not built.
 """
+from .binding import (FA_DTYPE_BF16, FA_DTYPE_F32, FA_ERR_ALIGNMENT, FA_ERR_CUDA,  # noqa: F401
+                      FA_ERR_INVALID_ARG, FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED, FA_OK, FAError,
+                      attention, fa_device_status, fa_fwd, fa_fwd_validate,
+                      fa_last_error_message, fa_status_string, fa_version)

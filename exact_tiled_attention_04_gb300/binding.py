@@ -1,0 +1,160 @@
+"""ctypes binding of the C ABI in include/fa.h (argument marshalling only).
+
+The functions here carry the C names and pass plain integers (device
+addresses, sizes) straight through; every step of the attention forward pass
+runs in the CUDA library.  If the library is missing the calls raise: there is
+no CPU fallback.
+
+``attention()`` is a convenience for PyTorch callers: it checks tensor
+shapes/dtypes, allocates the outputs with PyTorch (the library itself never
+allocates) and calls ``fa_fwd`` on the current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfa_gb300.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "fa.h")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_ALIGNMENT = 3
+FA_ERR_CUDA = 4
+FA_ERR_TIMEOUT = 5
+FA_DTYPE_F32 = 0
+FA_DTYPE_BF16 = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {fa_status_string(status)} (status {status})"
+        detail = fa_last_error_message()
+        if detail:
+            msg += f"; {detail}"
+        super().__init__(msg)
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load the CUDA library (once).  Raises if it was not built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = path or LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA attention library not found at {path}; build it with "
+                "`python -m exact_tiled_attention_04_gb300.build` (there is no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        i64, vp, f32, c_int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
+        lib.fa_fwd.restype = c_int
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, f32, c_int, vp]
+        lib.fa_fwd_validate.restype = c_int
+        lib.fa_fwd_validate.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, f32, c_int]
+        lib.fa_device_status.restype = c_int
+        lib.fa_device_status.argtypes = [vp]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_status_string.argtypes = [c_int]
+        lib.fa_last_error_message.restype = ctypes.c_char_p
+        lib.fa_last_error_message.argtypes = []
+        lib.fa_version.restype = c_int
+        lib.fa_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/fa.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(fa_\w+)\s*\(", text, flags=re.M)
+
+
+# ----------------------------------------------------------- C-ABI mirrors
+def fa_fwd(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, N: int, d: int,
+           scale: float, dtype: int, stream: int | None) -> int:
+    return load().fa_fwd(q, k, v, o, lse or None, B, H, N, d, scale, dtype, stream or None)
+
+
+def fa_fwd_validate(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, N: int,
+                    d: int, scale: float, dtype: int) -> int:
+    return load().fa_fwd_validate(q, k, v, o, lse or None, B, H, N, d, scale, dtype)
+
+
+def fa_device_status(stream: int | None) -> int:
+    return load().fa_device_status(stream or None)
+
+
+def fa_status_string(status: int) -> str:
+    return load().fa_status_string(status).decode()
+
+
+def fa_last_error_message() -> str:
+    return load().fa_last_error_message().decode()
+
+
+def fa_version() -> int:
+    return load().fa_version()
+
+
+# ------------------------------------------------------- PyTorch convenience
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return FA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return FA_DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: bfloat16 or float32")
+
+
+def attention(q, k, v, scale: float | None = None, out=None, lse=None, with_lse: bool = True,
+              stream=None):
+    """O = softmax(scale * Q K^T) V for CUDA tensors [B, H, N, d].
+
+    Returns (out, lse); lse is fp32 [B, H, N] (natural log) or None when
+    with_lse is False.  scale defaults to 1/sqrt(d) in fp32.  Enqueued on
+    `stream` (default: PyTorch's current stream); raises FAError on a
+    non-OK status.
+    """
+    import torch
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError(f"q, k, v must share one [B,H,N,d] shape: {q.shape} {k.shape} {v.shape}")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share a dtype")
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous")
+    B, H, N, d = (int(x) for x in q.shape)
+    if scale is None:
+        scale = float(torch.tensor(1.0, dtype=torch.float32) / torch.sqrt(torch.tensor(float(d), dtype=torch.float32)))
+    if not math.isfinite(scale):
+        raise ValueError("scale must be finite")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and with_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                    lse.data_ptr() if lse is not None else None, B, H, N, d, float(scale),
+                    _dtype_code(q), s.cuda_stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_fwd")
+    return out, lse

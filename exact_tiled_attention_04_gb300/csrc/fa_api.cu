@@ -1,0 +1,227 @@
+// C-ABI entry points of the attention library (declared in include/fa.h):
+// host-side argument checks, TMA tensor-map encoding, kernel dispatch and
+// the device error word.
+//
+// The boundary follows the fused kernel of "CUDA Flash Attention: Online
+// Softmax with Shared Memory Tiling" (Kernel 2: Q, K, V, O, N, d and scale
+// as arguments; Design decisions: size_t indexing, restrict-qualified
+// non-aliasing outputs; Correctness Audit: launch errors surfaced, the head
+// dimension checked instead of assumed), extended with batch, heads, dtype,
+// the log-sum-exp output and a stream.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+// Set by the kernels when a bounded wait gives up (one word per device).
+__device__ unsigned int g_fa_device_error;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+void set_error(const char* what, int code, const char* text) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s: error %d (%s)", what, code,
+                  text ? text : "");
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                        cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+constexpr int kMaxDevices = 64;
+unsigned int* g_err_ptr[kMaxDevices] = {};
+std::mutex g_err_mutex;
+
+// Device address of the error word on the current device.
+unsigned int* device_error_word(int* status) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        set_error("cudaGetDevice", static_cast<int>(e), cudaGetErrorString(e));
+        *status = FA_ERR_CUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_err_mutex);
+    if (g_err_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fa_device_error);
+        if (e != cudaSuccess) {
+            set_error("cudaGetSymbolAddress", static_cast<int>(e), cudaGetErrorString(e));
+            *status = FA_ERR_CUDA;
+            return nullptr;
+        }
+        g_err_ptr[dev] = static_cast<unsigned int*>(p);
+    }
+    *status = FA_OK;
+    return g_err_ptr[dev];
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// 3-D tiled map over [BH, N, d] (innermost first), 128-byte swizzle, boxes of
+// 128 bytes x 128 rows x 1 head; rows past N read as zero and are not written.
+int encode_map(CUtensorMap* map, const void* base, int dtype, int64_t BH, int64_t N, int64_t d) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (enc == nullptr) {
+        set_error("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)",
+                  static_cast<int>(g_encode_err), cudaGetErrorString(g_encode_err));
+        return FA_ERR_CUDA;
+    }
+    const cuuint64_t elem = dtype == FA_DTYPE_BF16 ? 2 : 4;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elem,
+                                   static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * elem};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem), 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map,
+                     dtype == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                     3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_error("cuTensorMapEncodeTiled", static_cast<int>(r), "tensor map rejected");
+        return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
+constexpr int64_t kInt32Max = 2147483647;
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char* fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "ok";
+        case FA_ERR_INVALID_ARG: return "invalid argument";
+        case FA_ERR_UNSUPPORTED: return "unsupported head dimension, dtype or size";
+        case FA_ERR_ALIGNMENT: return "tensor base address not 16-byte aligned";
+        case FA_ERR_CUDA: return "CUDA call failed";
+        case FA_ERR_TIMEOUT: return "kernel timed out waiting on an internal barrier";
+        default: return "unknown status";
+    }
+}
+
+const char* fa_last_error_message(void) { return g_last_error; }
+
+int fa_fwd_validate(const void* q, const void* k, const void* v, void* o, const float* lse,
+                    int64_t B, int64_t H, int64_t N, int64_t d, float scale, int dtype) {
+    if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
+    if (dtype == FA_DTYPE_BF16 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (dtype == FA_DTYPE_F32 && d != 64) return FA_ERR_UNSUPPORTED;
+    // element count and byte size must fit in int64 (d is 64 or 128 here)
+    if (B > INT64_MAX / H) return FA_ERR_INVALID_ARG;
+    const int64_t BH = B * H;
+    if (BH > INT64_MAX / N || BH * N > INT64_MAX / (d * 4)) return FA_ERR_INVALID_ARG;
+    // TMA coordinates are 32-bit; global strides below 2^40 bytes
+    if (BH > kInt32Max || N > kInt32Max) return FA_ERR_UNSUPPORTED;
+    const int64_t elem = dtype == FA_DTYPE_BF16 ? 2 : 4;
+    if (N * d * elem >= (int64_t(1) << 40)) return FA_ERR_UNSUPPORTED;
+    const int64_t qblocks = (N + 255) / 256;
+    if (qblocks > kInt32Max / BH) return FA_ERR_UNSUPPORTED;  // one CTA per 256 rows
+    const uintptr_t mask = 15;
+    if ((reinterpret_cast<uintptr_t>(q) & mask) || (reinterpret_cast<uintptr_t>(k) & mask) ||
+        (reinterpret_cast<uintptr_t>(v) & mask) || (reinterpret_cast<uintptr_t>(o) & mask))
+        return FA_ERR_ALIGNMENT;
+    if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3)) return FA_ERR_ALIGNMENT;
+    const size_t bytes = static_cast<size_t>(BH * N * d * elem);
+    if (overlaps(o, bytes, q, bytes) || overlaps(o, bytes, k, bytes) || overlaps(o, bytes, v, bytes))
+        return FA_ERR_INVALID_ARG;
+    if (lse != nullptr) {
+        const size_t lbytes = static_cast<size_t>(BH * N) * sizeof(float);
+        if (overlaps(lse, lbytes, o, bytes) || overlaps(lse, lbytes, q, bytes) ||
+            overlaps(lse, lbytes, k, bytes) || overlaps(lse, lbytes, v, bytes))
+            return FA_ERR_INVALID_ARG;
+    }
+    return FA_OK;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+           int64_t N, int64_t d, float scale, int dtype, void* stream) {
+    int st = fa_fwd_validate(q, k, v, o, lse, B, H, N, d, scale, dtype);
+    if (st != FA_OK) return st;
+    const int64_t BH = B * H;
+    CUtensorMap mq, mk, mv, mo;
+    if ((st = encode_map(&mq, q, dtype, BH, N, d)) != FA_OK) return st;
+    if ((st = encode_map(&mk, k, dtype, BH, N, d)) != FA_OK) return st;
+    if ((st = encode_map(&mv, v, dtype, BH, N, d)) != FA_OK) return st;
+    if ((st = encode_map(&mo, o, dtype, BH, N, d)) != FA_OK) return st;
+
+    fa::FwdParams p;
+    p.lse = lse;
+    p.err = device_error_word(&st);
+    if (st != FA_OK) return st;
+    p.N = static_cast<int>(N);
+    p.n_kv_tiles = static_cast<int>((N + 127) / 128);
+    p.n_q_blocks = static_cast<int>((N + 255) / 256);
+    p.scale_log2 = scale * 1.4426950408889634f;
+    const unsigned int grid = static_cast<unsigned int>(BH * p.n_q_blocks);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    cudaError_t e;
+    if (dtype == FA_DTYPE_BF16 && d == 64)
+        e = fa::launch_fwd_bf16_d64(mq, mk, mv, mo, p, grid, s);
+    else if (dtype == FA_DTYPE_BF16)
+        e = fa::launch_fwd_bf16_d128(mq, mk, mv, mo, p, grid, s);
+    else
+        e = fa::launch_fwd_tf32_d64(mq, mk, mv, mo, p, grid, s);
+    if (e != cudaSuccess) {
+        set_error("fa_fwd launch", static_cast<int>(e), cudaGetErrorString(e));
+        return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
+int fa_device_status(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        set_error("cudaStreamSynchronize", static_cast<int>(e), cudaGetErrorString(e));
+        return FA_ERR_CUDA;
+    }
+    unsigned int word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_fa_device_error, sizeof(word));
+    if (e != cudaSuccess) {
+        set_error("cudaMemcpyFromSymbol", static_cast<int>(e), cudaGetErrorString(e));
+        return FA_ERR_CUDA;
+    }
+    if (word == 0) return FA_OK;
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_fa_device_error, &zero, sizeof(zero));
+    if (e != cudaSuccess) {
+        set_error("cudaMemcpyToSymbol", static_cast<int>(e), cudaGetErrorString(e));
+        return FA_ERR_CUDA;
+    }
+    std::snprintf(g_last_error, sizeof(g_last_error), "device error word 0x%08x", word);
+    return (word & fa::kDevErrTimeout) ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
+}
+
+}  // extern "C"

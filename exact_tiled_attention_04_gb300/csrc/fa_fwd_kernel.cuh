@@ -1,0 +1,734 @@
+// Fused exact-attention forward kernel for sm_103a (GB300).
+//
+// What it computes ("How Did I Write My First FlashAttention Kernel in
+// CUDA?", pseudo-algorithm steps 1-5; "FlashAttention dissected", section
+// "Algorithmic core in pseudocode"): for a block of query rows, sweep the
+// key/value sequence tile by tile, keeping per row a running maximum m, a
+// running denominator l and an unnormalised output accumulator O that is
+// rescaled by exp(m_old - m_new) whenever m moves; divide O by l once at the
+// end ("FlashAttention dissected", the final normalisation after the inner
+// loop; the deferred division of "CUDA Flash Attention: Online Softmax with
+// Shared Memory Tiling", Kernel 2).  The N x N score matrix never leaves the
+// SM.
+//
+// Organisation (one CTA = 256 query rows of one (batch, head), 320 threads):
+//   warps 0-3  softmax warpgroup 0: query tile 0 (rows 0-127 of the block)
+//   warps 4-7  softmax warpgroup 1: query tile 1 (rows 128-255)
+//   warp  8    tensor-core issuer (one thread) and TMEM owner
+//   warp  9    TMA producer (one thread)
+// Tensor memory (512 columns x 128 lanes, fp32):
+//   S_w  columns [128w, 128w+128)   scores of tile w; P_w overwrites its
+//                                   first columns (bf16 pairs or tf32)
+//   O_w  columns [256 + Dw, 256 + D(w+1))   output accumulator of tile w
+// Shared memory (128-byte-swizzled TMA tiles, 1024-byte aligned):
+//   Q_0, Q_1 (reused as the output staging tiles), a ring of K tiles and a
+//   ring of V tiles, then the mbarriers.
+// Tensor-core schedule per key tile j (w = 0, 1 alternate, so the softmax of
+// one tile overlaps the matrix products of the other):
+//   S_0(j) = Q_0 K_j^T   S_1(j) = Q_1 K_j^T   O_0 += P_0(j) V_j
+//   S_0(j+1)             O_1 += P_1(j) V_j    S_1(j+1) ...
+//
+// Online-softmax details:
+//   * scores are handled in base 2: t = s * scale * log2(e), p = 2^(t - m);
+//   * the reference maximum m is only moved when the tile maximum exceeds
+//     it by more than 8 (a factor 256): O and l are rescaled then, and
+//     otherwise p <= 2^8 with the stale m.  The final O / l and
+//     lse = (m + log2 l) ln 2 are exact for any reference maximum;
+//   * keys past N in the last tile get weight exactly 0 (the "tile masking"
+//     of "CUDA Flash Attention: Online Softmax with Shared Memory Tiling",
+//     Design decisions, with the masked keys excluded rather than given a
+//     large negative score); a reference maximum of -inf is replaced by 0
+//     so that (-inf) - (-inf) never occurs (that page's NaN guard).
+//
+// Every wait on an mbarrier is bounded: after about a second the waiting
+// thread raises a CTA-wide abort flag and sets the device error word; every
+// role then leaves its loop, in-flight tensor-core work and TMA loads are
+// drained, and tensor memory is freed before the CTA exits.
+#pragma once
+
+#include <cmath>
+#include <cstdint>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+constexpr int kTileM = 128;  // query rows per softmax warpgroup = TMEM lanes
+constexpr int kTileN = 128;  // keys per K/V tile
+// Three warpgroups: two softmax warpgroups and one holding the tensor-core
+// issuer warp, the TMA warp and two idle warps.  Registers are allocated per
+// warpgroup, so the launch gets 384 x 168; setmaxnreg then moves them to
+// the softmax warpgroups (2 x 128 x 216 + 128 x 72 = 384 x 168).
+constexpr int kThreads = 384;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr uint32_t kLaunchRegs = 168;
+constexpr uint32_t kSoftmaxRegs = 216;
+constexpr uint32_t kOtherRegs = 72;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs == kThreads * kLaunchRegs,
+              "register split must equal the launch allocation");
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;             // log2 units
+constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+
+template <bool TF32, int D>
+struct FwdCfg {
+    static constexpr int kElem = TF32 ? 4 : 2;
+    static constexpr int kAtomElems = 128 / kElem;      // elements in one 128-byte swizzle row
+    static constexpr int kAtoms = D / kAtomElems;       // swizzle atoms across the head dim
+    static constexpr int kAtomBytes = 128 * 128;        // 128 rows x 128 bytes
+    static constexpr int kTileBytes = kAtoms * kAtomBytes;
+    static constexpr int kUmmaK = 32 / kElem;           // K of one MMA instruction (32 bytes)
+    static constexpr int kQkSteps = D / kUmmaK;
+    static constexpr int kPvSteps = kTileN / kUmmaK;
+    // fp32 inputs: the K ring holds TF32-rounded tiles, the V ring holds
+    // transposed V^T tiles (the TF32 kind takes K-major operands only), and
+    // one extra buffer receives the raw V tile from TMA.
+    static constexpr int kKStages = TF32 ? 2 : (kTileBytes <= 16384 ? 4 : 3);
+    static constexpr int kVStages = TF32 ? 2 : (kTileBytes <= 16384 ? 4 : 2);
+    static constexpr int kVtAtomBytes = D * 128;  // V^T: D rows x 32 keys (128 bytes)
+    static constexpr uint32_t kFmt = TF32 ? 2u : 1u;
+    // S = Q K^T: M = 128, N = 128, A and B K-major.
+    static constexpr uint32_t kIdescQK = instr_desc(kFmt, false, false, kTileM, kTileN);
+    // O += P V: A (P) from TMEM, B (V) MN-major, M = 128.  bf16: one
+    // instruction per k-step covers the whole head dimension (N = D; the
+    // 64-column blocks of V are kAtomBytes apart, the descriptor's leading
+    // byte offset).  Every tcgen05.mma costs about the same time for any
+    // N <= 128, so fewer, wider instructions are faster.
+    static constexpr int kPvN = D;
+    static constexpr int kPvSplit = 1;
+    static constexpr uint32_t kIdescPV = instr_desc(kFmt, false, !TF32, kTileM, kPvN);
+
+    // shared-memory map (offsets from the 1024-aligned base)
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+    static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+    static constexpr int kOffVRaw = kOffV + kVStages * kTileBytes;
+    static constexpr int kOffBar = kOffVRaw + (TF32 ? kTileBytes : 0);
+    // barrier slots
+    static constexpr int kBarQFull = 0;
+    static constexpr int kBarKFull = 1;
+    static constexpr int kBarKEmpty = kBarKFull + kKStages;
+    static constexpr int kBarVFull = kBarKEmpty + kKStages;
+    static constexpr int kBarVEmpty = kBarVFull + kVStages;
+    static constexpr int kBarSFull = kBarVEmpty + kVStages;  // [2]
+    static constexpr int kBarPFull = kBarSFull + 2;          // [2]
+    static constexpr int kBarOFull = kBarPFull + 2;          // [2]
+    static constexpr int kBarEpi = kBarOFull + 2;            // [2]
+    static constexpr int kBarDrain = kBarEpi + 2;
+    static constexpr int kBarQRaw = kBarDrain + 1;  // fp32 only: TMA landed, not yet rounded
+    static constexpr int kBarKRaw = kBarQRaw + 1;   // [kKStages]
+    static constexpr int kBarVRaw = kBarKRaw + kKStages;
+    static constexpr int kNumBars = kBarVRaw + 1;
+    static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+    static constexpr int kOffAbort = kOffTmemSlot + 4;
+    static constexpr int kSmemUsed = kOffAbort + 4;
+    static constexpr size_t kSmemBytes = static_cast<size_t>(kSmemUsed) + 1024;  // alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
+    static_assert(256 + 2 * D <= static_cast<int>(kTmemCols), "tensor memory budget exceeded");
+};
+
+// Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting
+// (if `honor_abort`) or when this wait itself gave up after kWaitLimitNs, in
+// which case it raises the abort flag and the device error word.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
+                                           volatile uint32_t* abort_flag, unsigned int* err,
+                                           unsigned int where, bool honor_abort = true) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    uint32_t spins = 0;
+    while (true) {
+        if (mbar_test(bar, parity)) return true;
+        if ((++spins & 31u) == 0u) {
+            if (honor_abort && *abort_flag) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1u;
+                atomicOr(err, kDevErrTimeout | (where << 8));
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+// Maximum (kMax) or minimum of a 128-key score row held in registers: eight
+// running accumulators over keys k = a (mod 8), three-input max/min, so only
+// eight values are live beside the row and the dependent chain is 8 long.
+template <bool kMax>
+__device__ __forceinline__ float row_extreme(const uint32_t (&s)[4][32]) {
+    auto v = [&](int e) { return u2f(s[e / 32][e % 32]); };
+    auto two = [](float a, float b) { return kMax ? fmaxf(a, b) : fminf(a, b); };
+    auto three = [](float a, float b, float c) { return kMax ? fmax3(a, b, c) : fmin3(a, b, c); };
+    float acc[8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a) acc[a] = two(v(a), v(a + 8));
+#pragma unroll
+    for (int r = 2; r < 16; r += 2)
+#pragma unroll
+        for (int a = 0; a < 8; ++a) acc[a] = three(acc[a], v(a + 8 * r), v(a + 8 * (r + 1)));
+    return two(three(acc[0], acc[1], acc[2]), three(acc[3], acc[4], two(acc[5], three(acc[6], acc[7], acc[7]))));
+}
+
+// Softmax numerators of one 128-key score row held in registers:
+// p_j = 2^(s_j * c - shift), keys >= `valid` get p = 0 (kMasked, last tile
+// only).  Writes P into tensor memory at `tS` (bf16 pairs, or TF32 values one
+// per column) and adds sum p (fp32) to l and the sum of the rounded p, the
+// weights the P V product actually uses, to lq.  Pairs of keys go through the
+// packed f32x2 FMA / add; eight independent partial sums.
+template <bool TF32, bool kMasked>
+__device__ __forceinline__ void exp_tile(const uint32_t (&s)[4][32], float c, float shift, int valid,
+                                         uint32_t tS, float& l, float& lq) {
+    const uint64_t c2 = f2_pack(c, c);
+    const uint64_t ns2 = f2_pack(-shift, -shift);
+    uint64_t acc[4] = {0, 0, 0, 0};
+    uint64_t qacc[4] = {0, 0, 0, 0};
+    if constexpr (TF32) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t pw[32];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                float t0, t1;
+                f2_unpack(f2_fma(f2_pack(u2f(s[q][i]), u2f(s[q][i + 1])), c2, ns2), t0, t1);
+                float p0 = ex2(t0), p1 = ex2(t1);
+                if constexpr (kMasked) {
+                    if (q * 32 + i >= valid) p0 = 0.0f;
+                    if (q * 32 + i + 1 >= valid) p1 = 0.0f;
+                }
+                pw[i] = round_tf32(p0);
+                pw[i + 1] = round_tf32(p1);
+                acc[(i / 2) & 3] = f2_add(acc[(i / 2) & 3], f2_pack(p0, p1));
+                qacc[(i / 2) & 3] = f2_add(qacc[(i / 2) & 3], f2_pack(u2f(pw[i]), u2f(pw[i + 1])));
+            }
+            tmem_st32(tS + 32u * q, pw);
+        }
+    } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t pw[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int c0 = h * 64 + 2 * i;  // keys c0, c0 + 1
+                float t0, t1;
+                f2_unpack(f2_fma(f2_pack(u2f(s[c0 / 32][c0 % 32]), u2f(s[c0 / 32][c0 % 32 + 1])), c2, ns2),
+                          t0, t1);
+                float p0 = ex2(t0), p1 = ex2(t1);
+                if constexpr (kMasked) {
+                    if (c0 >= valid) p0 = 0.0f;
+                    if (c0 + 1 >= valid) p1 = 0.0f;
+                }
+                const uint32_t pk = pack_bf16x2(p0, p1);
+                pw[i] = pk;
+                acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+                qacc[i & 3] = f2_add(qacc[i & 3], f2_pack(u2f(pk << 16), u2f(pk & 0xFFFF0000u)));
+            }
+            tmem_st32(tS + 32u * h, pw);
+        }
+    }
+    float a[8], b[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        f2_unpack(acc[k], a[2 * k], a[2 * k + 1]);
+        f2_unpack(qacc[k], b[2 * k], b[2 * k + 1]);
+    }
+    l += ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+    lq += ((b[0] + b[1]) + (b[2] + b[3])) + ((b[4] + b[5]) + (b[6] + b[7]));
+}
+
+// Round `n16` 16-byte groups of fp32 in shared memory to TF32 in place
+// (round to nearest, ties away), one warp.
+__device__ __forceinline__ void round_tf32_inplace(uint8_t* base, int n16, int lane) {
+#pragma unroll 1
+    for (int i = lane; i < n16; i += 32) {
+        uint4* p4 = reinterpret_cast<uint4*>(base) + i;
+        uint4 v = *p4;
+        v.x = round_tf32(u2f(v.x));
+        v.y = round_tf32(u2f(v.y));
+        v.z = round_tf32(u2f(v.z));
+        v.w = round_tf32(u2f(v.w));
+        *p4 = v;
+    }
+}
+
+// fp32 V tile as loaded by TMA ([D/32 atoms][128 keys][128 bytes], swizzled)
+// -> TF32-rounded V^T in the K-major swizzled operand layout
+// ([4 atoms of 32 keys][D rows][128 bytes]).  Iteration i: lanes cover 32
+// consecutive d of one key group, so the reads are 4 row-contiguous 128-byte
+// lines and the 16-byte writes take the minimum 4 wavefronts.
+template <int D>
+__device__ __forceinline__ void transpose_v_tf32(const uint8_t* vraw, uint8_t* vt, int lane) {
+    constexpr int kDBlocks = D / 32;
+#pragma unroll 1
+    for (int i = 0; i < 32 * kDBlocks; ++i) {
+        const int d = (i % kDBlocks) * 32 + lane;
+        const int kg = i / kDBlocks;  // keys 4kg .. 4kg+3
+        const int atom_in = d / 32, c_in = (d % 32) / 4, w_in = (d % 4) * 4;
+        uint32_t r[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int key = 4 * kg + t;
+            const uint8_t* src = vraw + atom_in * 16384 + key * 128 + ((c_in ^ (key & 7)) << 4) + w_in;
+            r[t] = round_tf32(*reinterpret_cast<const float*>(src));
+        }
+        uint8_t* dst = vt + (kg / 8) * (D * 128) + d * 128 + (((kg % 8) ^ (d & 7)) << 4);
+        *reinterpret_cast<uint4*>(dst) = make_uint4(r[0], r[1], r[2], r[3]);
+    }
+}
+
+// Producer warp of the fp32 (TF32) variant: TMA loads as in the bf16 path,
+// then the whole warp rounds Q and K tiles in place and writes V^T tiles,
+// each published on its own barrier after a proxy fence.
+template <int D>
+__device__ void produce_tf32(const CUtensorMap& map_q, const CUtensorMap& map_k,
+                             const CUtensorMap& map_v, const FwdParams& p, uint8_t* smem,
+                             uint32_t sbase, int lane, int row0, int bh, int T,
+                             volatile uint32_t* abort_flag) {
+    using C = FwdCfg<true, D>;
+    auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * static_cast<uint32_t>(i); };
+    auto all_ok = [&](bool ok) { return __all_sync(0xffffffffu, ok); };
+    const uint64_t keep = policy_evict_last();
+    const uint64_t once = policy_evict_first();
+    int nk = 0, nv = 0;  // K and V tiles whose loads were issued
+    bool q_issued = false;
+    bool ok = true;
+    if (lane == 0) {
+        mbar_arrive_expect_tx(bar(C::kBarQRaw), 2u * C::kTileBytes);
+        for (int w = 0; w < 2; ++w)
+            for (int a = 0; a < C::kAtoms; ++a)
+                tma_load_3d(sbase + C::kOffQ + w * C::kTileBytes + a * C::kAtomBytes, &map_q,
+                            bar(C::kBarQRaw), a * C::kAtomElems, row0 + w * kTileM, bh, once);
+    }
+    q_issued = true;
+    ok = all_ok(wait_phase(bar(C::kBarQRaw), 0, abort_flag, p.err, 20));
+    if (ok) {
+        round_tf32_inplace(smem + C::kOffQ, 2 * C::kTileBytes / 16, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::kBarQFull));
+    }
+    for (int j = 0; ok && j < T; ++j) {
+        const int ks = j % C::kKStages;
+        const int vs = j % C::kVStages;
+        ok = all_ok(wait_phase(bar(C::kBarKEmpty + ks), ((j / C::kKStages) & 1) ^ 1, abort_flag, p.err, 21));
+        if (!ok) break;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(C::kBarKRaw + ks), C::kTileBytes);
+            for (int a = 0; a < C::kAtoms; ++a)
+                tma_load_3d(sbase + C::kOffK + ks * C::kTileBytes + a * C::kAtomBytes, &map_k,
+                            bar(C::kBarKRaw + ks), a * C::kAtomElems, j * kTileN, bh, keep);
+            // the raw V buffer was fully read by this warp's previous transpose
+            mbar_arrive_expect_tx(bar(C::kBarVRaw), C::kTileBytes);
+            for (int a = 0; a < C::kAtoms; ++a)
+                tma_load_3d(sbase + C::kOffVRaw + a * C::kAtomBytes, &map_v, bar(C::kBarVRaw),
+                            a * C::kAtomElems, j * kTileN, bh, keep);
+        }
+        nk = j + 1;
+        nv = j + 1;
+        ok = all_ok(wait_phase(bar(C::kBarKRaw + ks), (j / C::kKStages) & 1, abort_flag, p.err, 22));
+        if (!ok) break;
+        round_tf32_inplace(smem + C::kOffK + ks * C::kTileBytes, C::kTileBytes / 16, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::kBarKFull + ks));
+        ok = all_ok(wait_phase(bar(C::kBarVRaw), j & 1, abort_flag, p.err, 23));
+        if (!ok) break;
+        ok = all_ok(wait_phase(bar(C::kBarVEmpty + vs), ((j / C::kVStages) & 1) ^ 1, abort_flag, p.err, 24));
+        if (!ok) break;
+        transpose_v_tf32<D>(smem + C::kOffVRaw, smem + C::kOffV + vs * C::kTileBytes, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::kBarVFull + vs));
+    }
+    // Drain every TMA load this warp issued (see the bf16 producer).
+    if (lane == 0) {
+        if (q_issued) wait_phase(bar(C::kBarQRaw), 0, abort_flag, p.err, 25, false);
+        for (int s = 0; s < C::kKStages && s < nk; ++s) {
+            const int last = s + ((nk - 1 - s) / C::kKStages) * C::kKStages;
+            wait_phase(bar(C::kBarKRaw + s), (last / C::kKStages) & 1, abort_flag, p.err, 25, false);
+        }
+        if (nv > 0) wait_phase(bar(C::kBarVRaw), (nv - 1) & 1, abort_flag, p.err, 25, false);
+    }
+}
+
+template <bool TF32, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
+                  const FwdParams p) {
+    using C = FwdCfg<TF32, D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_u32 & 1023u)) & 1023u;
+    uint8_t* smem = smem_raw + pad;
+    const uint32_t sbase = raw_u32 + pad;
+
+    const int warp = static_cast<int>(threadIdx.x) / 32;
+    const int lane = static_cast<int>(threadIdx.x) % 32;
+    const int qb = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.n_q_blocks));
+    const int bh = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.n_q_blocks));
+    const int row0 = qb * 2 * kTileM;
+    const int T = p.n_kv_tiles;
+
+    auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * static_cast<uint32_t>(i); };
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kOffAbort);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemSlot);
+
+    // ---------------------------------------------------------------- setup
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::kBarQFull), 1);
+        for (int s = 0; s < C::kKStages; ++s) {
+            mbar_init(bar(C::kBarKFull + s), 1);
+            mbar_init(bar(C::kBarKEmpty + s), 1);
+        }
+        for (int s = 0; s < C::kVStages; ++s) {
+            mbar_init(bar(C::kBarVFull + s), 1);
+            mbar_init(bar(C::kBarVEmpty + s), 1);
+        }
+        for (int w = 0; w < 2; ++w) {
+            mbar_init(bar(C::kBarSFull + w), 1);
+            mbar_init(bar(C::kBarPFull + w), 4);  // one arrival per softmax warp
+            mbar_init(bar(C::kBarOFull + w), 1);
+            mbar_init(bar(C::kBarEpi + w), kTileM);
+        }
+        mbar_init(bar(C::kBarDrain), 1);
+        mbar_init(bar(C::kBarQRaw), 1);
+        for (int s = 0; s < C::kKStages; ++s) mbar_init(bar(C::kBarKRaw + s), 1);
+        mbar_init(bar(C::kBarVRaw), 1);
+        // A CTA starting after another one timed out does no work.
+        *abort_flag = (*reinterpret_cast<volatile unsigned int*>(p.err) != 0u) ? 1u : 0u;
+        mbar_init_fence();
+    }
+    if (warp == kLoadWarp && lane == 0) {
+        tma_prefetch_desc(&map_q);
+        tma_prefetch_desc(&map_k);
+        tma_prefetch_desc(&map_v);
+        tma_prefetch_desc(&map_o);
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const bool skip = *abort_flag != 0u;
+    if (skip) {
+        // nothing issued: go straight to the teardown
+    } else if (warp >= 8) {
+        // warpgroup 2: TMA producer, tensor-core issuer, two idle warps
+        regs_decrease<kOtherRegs>();
+      if (warp == kLoadWarp) {
+        // ------------------------------------------------------ TMA producer
+        if constexpr (TF32) {
+            produce_tf32<D>(map_q, map_k, map_v, p, smem, sbase, lane, row0, bh, T, abort_flag);
+        } else if (lane == 0) {
+            const uint64_t keep = policy_evict_last();   // K/V: read by every query block of the head
+            const uint64_t once = policy_evict_first();  // Q: read once
+            mbar_arrive_expect_tx(bar(C::kBarQFull), 2u * C::kTileBytes);
+            for (int w = 0; w < 2; ++w)
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_3d(sbase + C::kOffQ + w * C::kTileBytes + a * C::kAtomBytes, &map_q,
+                                bar(C::kBarQFull), a * C::kAtomElems, row0 + w * kTileM, bh, once);
+            int nk = 0, nv = 0;  // K and V tiles whose loads were issued
+            for (int j = 0; j < T; ++j) {
+                const int ks = j % C::kKStages;
+                if (!wait_phase(bar(C::kBarKEmpty + ks), ((j / C::kKStages) & 1) ^ 1, abort_flag, p.err, 1))
+                    break;
+                mbar_arrive_expect_tx(bar(C::kBarKFull + ks), C::kTileBytes);
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_3d(sbase + C::kOffK + ks * C::kTileBytes + a * C::kAtomBytes, &map_k,
+                                bar(C::kBarKFull + ks), a * C::kAtomElems, j * kTileN, bh, keep);
+                nk = j + 1;
+                const int vs = j % C::kVStages;
+                if (!wait_phase(bar(C::kBarVEmpty + vs), ((j / C::kVStages) & 1) ^ 1, abort_flag, p.err, 2))
+                    break;
+                mbar_arrive_expect_tx(bar(C::kBarVFull + vs), C::kTileBytes);
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_3d(sbase + C::kOffV + vs * C::kTileBytes + a * C::kAtomBytes, &map_v,
+                                bar(C::kBarVFull + vs), a * C::kAtomElems, j * kTileN, bh, keep);
+                nv = j + 1;
+            }
+            // Drain: wait until every issued load has landed, so that no TMA
+            // write reaches shared memory after the CTA exits.  On the normal
+            // path these phases completed long ago.  The last tile loaded
+            // into stage s is the largest index below the issued count that
+            // is congruent to s.
+            wait_phase(bar(C::kBarQFull), 0, abort_flag, p.err, 3, false);
+            for (int s = 0; s < C::kKStages && s < nk; ++s) {
+                const int last = s + ((nk - 1 - s) / C::kKStages) * C::kKStages;
+                wait_phase(bar(C::kBarKFull + s), (last / C::kKStages) & 1, abort_flag, p.err, 3, false);
+            }
+            for (int s = 0; s < C::kVStages && s < nv; ++s) {
+                const int last = s + ((nv - 1 - s) / C::kVStages) * C::kVStages;
+                wait_phase(bar(C::kBarVFull + s), (last / C::kVStages) & 1, abort_flag, p.err, 3, false);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------- tensor-core issuer
+        if (lane == 0) {
+            auto issue_qk = [&](int w, int ks) {
+                const uint32_t dS = tmem + (w ? 128u : 0u);
+                const uint32_t sQ = sbase + C::kOffQ + (w ? C::kTileBytes : 0);
+                const uint32_t sK = sbase + C::kOffK + ks * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < C::kQkSteps; ++kk) {
+                    const uint32_t off = (kk * 32) / 128 * C::kAtomBytes + (kk * 32) % 128;
+                    const uint64_t da = smem_desc_sw128(sQ + off, 16, 1024);
+                    const uint64_t db = smem_desc_sw128(sK + off, 16, 1024);
+                    mma_ss<TF32>(dS, da, db, C::kIdescQK, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int w, int vs, bool accumulate) {
+                const uint32_t aP = tmem + (w ? 128u : 0u);
+                const uint32_t dO = tmem + 256u + (w ? static_cast<uint32_t>(D) : 0u);
+                const uint32_t sV = sbase + C::kOffV + vs * C::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < C::kPvSteps; ++kk) {
+                    uint64_t db;
+                    if constexpr (TF32) {
+                        // V^T, K-major: 32-key atoms of D rows; a k-step is 8 keys (32 bytes)
+                        db = smem_desc_sw128(sV + (kk / 4) * C::kVtAtomBytes + (kk % 4) * 32, 16, 1024);
+                    } else {
+                        // V, MN-major: 8-row groups 1024 bytes apart, 64-column blocks
+                        // kAtomBytes apart; a k-step is 16 rows
+                        db = smem_desc_sw128(sV + kk * C::kUmmaK * 128, C::kAtomBytes, 1024);
+                    }
+                    mma_ts<TF32>(dO, aP + kk * 8, db, C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+                }
+            };
+
+            bool ok = wait_phase(bar(C::kBarQFull), 0, abort_flag, p.err, 4);
+            if (ok) ok = wait_phase(bar(C::kBarKFull + 0), 0, abort_flag, p.err, 4);
+            if (ok) {
+                tc_fence_after();
+                issue_qk(0, 0);
+                tc_commit(bar(C::kBarSFull + 0));
+                issue_qk(1, 0);
+                tc_commit(bar(C::kBarSFull + 1));
+                tc_commit(bar(C::kBarKEmpty + 0));
+            }
+            for (int j = 0; ok && j < T; ++j) {
+                const int vs = j % C::kVStages;
+                const int ks = (j + 1) % C::kKStages;
+                ok = wait_phase(bar(C::kBarVFull + vs), (j / C::kVStages) & 1, abort_flag, p.err, 5);
+                if (!ok) break;
+                ok = wait_phase(bar(C::kBarPFull + 0), j & 1, abort_flag, p.err, 6);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(0, vs, j > 0);
+                if (j + 1 < T) {
+                    ok = wait_phase(bar(C::kBarKFull + ks), ((j + 1) / C::kKStages) & 1, abort_flag, p.err, 7);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_qk(0, ks);
+                    tc_commit(bar(C::kBarSFull + 0));
+                } else {
+                    tc_commit(bar(C::kBarOFull + 0));
+                }
+                ok = wait_phase(bar(C::kBarPFull + 1), j & 1, abort_flag, p.err, 8);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(1, vs, j > 0);
+                tc_commit(bar(C::kBarVEmpty + vs));
+                if (j + 1 < T) {
+                    issue_qk(1, ks);
+                    tc_commit(bar(C::kBarSFull + 1));
+                    tc_commit(bar(C::kBarKEmpty + ks));
+                } else {
+                    tc_commit(bar(C::kBarOFull + 1));
+                }
+            }
+            // Drain every tensor-core operation issued so far before the
+            // tensor memory is released.
+            tc_commit(bar(C::kBarDrain));
+            wait_phase(bar(C::kBarDrain), 0, abort_flag, p.err, 9, false);
+        }
+      }
+    } else {
+        // ------------------------------------------------ softmax warpgroups
+        regs_increase<kSoftmaxRegs>();
+        const int w = warp / 4;   // query tile of this warpgroup
+        const int wi = warp % 4;  // TMEM lane quarter this warp may access
+        const int t = wi * 32 + lane;  // row within the tile = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(wi * 32) << 16;
+        const uint32_t tS = tmem + lane_off + 128u * static_cast<uint32_t>(w);
+        const uint32_t tO = tmem + lane_off + 256u + static_cast<uint32_t>(D * w);
+        const float c = p.scale_log2;
+
+        float m_ref = -INFINITY;  // reference maximum, base-2 scaled units
+        float l = 0.0f;           // running sum of the weights p (fp32): gives lse
+        float lq = 0.0f;          // running sum of the weights as rounded for the
+                                  // product P V: O is divided by this one, so O is
+                                  // a convex combination of V rows with exactly the
+                                  // weights the tensor cores used
+        bool ok = true;
+
+        for (int j = 0; j < T; ++j) {
+            bool got = wait_phase(bar(C::kBarSFull + w), j & 1, abort_flag, p.err, 10);
+            ok = __all_sync(0xffffffffu, got);
+            if (!ok) break;
+            tc_fence_after();
+
+            uint32_t s[4][32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld32(tS + 32u * q, s[q]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld_wait(s[q]);
+
+            const int valid = p.N - j * kTileN;  // keys of this tile inside the sequence
+            if (valid < kTileN) {
+                // keys past N: copy key 0's score so they cannot win the max;
+                // their weight is zeroed below
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (q * 32 + i >= valid) s[q][i] = s[0][0];
+            }
+
+            // tile maximum of t = s * c (c may be negative or zero)
+            const float mx = (c >= 0.0f) ? row_extreme<true>(s) : row_extreme<false>(s);
+            const float m_tile = mx * c;
+            const float m_new = fmaxf(m_ref, m_tile);
+            const bool need = m_new > m_ref + kRescaleThreshold;  // always true on the first tile
+
+            // per-row factor for the accumulator (1 where the reference stays)
+            const float alpha = need ? ex2(m_ref - m_new) : 1.0f;
+            if (need) {
+                l *= alpha;  // alpha = 0 on the first tile (l was 0 anyway)
+                lq *= alpha;
+                m_ref = m_new;
+            }
+            const float shift = (m_ref == -INFINITY) ? 0.0f : m_ref;
+
+            // p = 2^(s*c - shift) for the 128 keys, two at a time (f32x2);
+            // P goes to TMEM over the scores, the sums stay in registers
+            if (valid < kTileN) {
+                exp_tile<TF32, true>(s, c, shift, valid, tS, l, lq);
+            } else {
+                exp_tile<TF32, false>(s, c, shift, valid, tS, l, lq);
+            }
+
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                // O holds the previous tiles' contributions (their products
+                // completed before this tile's scores were signalled); the
+                // next product into O waits for this warp's arrival below.
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + 32u * q, o);
+                    tmem_ld_wait(o);
+                    const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        float x0, x1;
+                        f2_unpack(f2_mul(f2_pack(u2f(o[i]), u2f(o[i + 1])), a2), x0, x1);
+                        o[i] = f2u(x0);
+                        o[i + 1] = f2u(x1);
+                    }
+                    tmem_st32(tO + 32u * q, o);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kBarPFull + w));
+        }
+
+        // ------------------------------------------------------- epilogue
+        if (ok) {
+            bool got = wait_phase(bar(C::kBarOFull + w), 0, abort_flag, p.err, 11);
+            ok = __all_sync(0xffffffffu, got);
+        }
+        const int row = row0 + w * kTileM + t;
+        uint8_t* stage = smem + C::kOffQ + w * C::kTileBytes;  // Q_w is free after its last S MMA
+        if (ok) {
+            tc_fence_after();
+            const float inv_l = lq > 0.0f ? 1.0f / lq : 0.0f;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                tmem_ld32(tO + 32u * q, o);
+                tmem_ld_wait(o);
+                if constexpr (TF32) {
+                    // 32 fp32 = one 128-byte swizzle row of atom q
+                    uint8_t* rowp = stage + q * C::kAtomBytes + t * 128;
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        uint4 v4;
+                        v4.x = f2u(u2f(o[4 * ch + 0]) * inv_l);
+                        v4.y = f2u(u2f(o[4 * ch + 1]) * inv_l);
+                        v4.z = f2u(u2f(o[4 * ch + 2]) * inv_l);
+                        v4.w = f2u(u2f(o[4 * ch + 3]) * inv_l);
+                        *reinterpret_cast<uint4*>(rowp + ((ch ^ (t & 7)) << 4)) = v4;
+                    }
+                } else {
+                    // 32 bf16 = half a swizzle row: chunks 4*(q%2) .. +3 of atom q/2
+                    uint8_t* rowp = stage + (q / 2) * C::kAtomBytes + t * 128;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int ch = (q % 2) * 4 + cc;
+                        uint4 v4;
+                        v4.x = pack_bf16x2(u2f(o[8 * cc + 0]) * inv_l, u2f(o[8 * cc + 1]) * inv_l);
+                        v4.y = pack_bf16x2(u2f(o[8 * cc + 2]) * inv_l, u2f(o[8 * cc + 3]) * inv_l);
+                        v4.z = pack_bf16x2(u2f(o[8 * cc + 4]) * inv_l, u2f(o[8 * cc + 5]) * inv_l);
+                        v4.w = pack_bf16x2(u2f(o[8 * cc + 6]) * inv_l, u2f(o[8 * cc + 7]) * inv_l);
+                        *reinterpret_cast<uint4*>(rowp + ((ch ^ (t & 7)) << 4)) = v4;
+                    }
+                }
+            }
+            if (p.lse != nullptr && row < p.N) {
+                const float lse2 = (l > 0.0f) ? (m_ref + log2f(l)) : -INFINITY;
+                p.lse[static_cast<size_t>(bh) * static_cast<size_t>(p.N) + row] = lse2 * 0.69314718055994531f;
+            }
+            fence_proxy_async_smem();
+        }
+        // Every thread of the warpgroup arrives exactly once, whatever happened.
+        mbar_arrive(bar(C::kBarEpi + w));
+        if (t == 0) {
+            const bool all_in = wait_phase(bar(C::kBarEpi + w), 0, abort_flag, p.err, 12);
+            // a tile lying entirely past N has nothing to store
+            if (all_in && !*abort_flag && row0 + w * kTileM < p.N) {
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_store_3d(&map_o, smem_u32(stage + a * C::kAtomBytes), a * C::kAtomElems,
+                                 row0 + w * kTileM, bh);
+                tma_store_commit();
+                tma_store_wait_read();
+            }
+        }
+    }
+
+    // --------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <bool TF32, int D>
+cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                       const CUtensorMap& o, const FwdParams& p, unsigned int grid,
+                       cudaStream_t stream) {
+    using C = FwdCfg<TF32, D>;
+    auto kern = fa_fwd_kernel<TF32, D>;
+    // The register split above relies on the compiled kernel holding exactly
+    // kLaunchRegs per thread; refuse to launch otherwise (a setmaxnreg.inc
+    // without the registers behind it would never return).
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(C::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(q, k, v, o, p);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

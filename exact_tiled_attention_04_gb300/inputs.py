@@ -169,6 +169,11 @@ WORKLOADS = {
         "long_n16384", 1, 8, 16384, 64, "bf16", seed=5, oracle_rows=256,
         note="N x N scores would be 1 GB per head; never materialised"),
 }
+# Half of the headline shape (134 MB of q, k, v, o: still larger than the
+# 129 MB L2); the case multi-pass profiler captures run on.
+WORKLOADS["b1h32_n8192_d128"] = Workload(
+    "b1h32_n8192_d128", 1, 32, 8192, 128, "bf16", seed=6, factor=0.5, oracle_rows=256,
+    note="profiling case: half the headline shape")
 HEADLINE = "b2h32_n8192_d128"
 SMALL = "single_head_n512"
 

@@ -1,0 +1,101 @@
+/*
+ * fa.h — fused exact-attention forward pass on GB300 (sm_103a), C ABI.
+ *
+ * The operation ("CUDA Flash Attention: Online Softmax with Shared Memory
+ * Tiling", Problem Statement; "FlashAttention dissected", section "Algorithmic
+ * core in pseudocode"): for every batch b, head h and query row i,
+ *
+ *     O[b,h,i,:] = sum_j softmax_j(scale * q_i . k_j) * v_j
+ *     lse[b,h,i] = log( sum_j exp(scale * q_i . k_j) )          (natural log)
+ *
+ * computed by one fused kernel that keeps a query tile on chip, sweeps the
+ * key/value sequence tile by tile with the online-softmax update (running
+ * maximum m, running denominator l, accumulator rescaled by exp(m_old - m_new);
+ * "How Did I Write My First FlashAttention Kernel in CUDA?", pseudo-algorithm
+ * steps 1-5) and never writes the N x N score matrix to memory.
+ *
+ * Every entry point is callable from C.  No torch type appears here.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes of every entry point. */
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,  /* NULL pointer, size < 1, overflow, non-finite scale */
+    FA_ERR_UNSUPPORTED = 2,  /* head dimension / dtype combination not built, size beyond TMA limits */
+    FA_ERR_ALIGNMENT = 3,    /* a tensor base address is not 16-byte aligned */
+    FA_ERR_CUDA = 4,         /* a CUDA runtime or driver call failed (see fa_last_error_message) */
+    FA_ERR_TIMEOUT = 5       /* a kernel gave up waiting on an internal barrier (device status) */
+} fa_status_t;
+
+/* Element type of q, k, v and o. */
+typedef enum {
+    FA_DTYPE_F32 = 0,   /* fp32 in/out; the two contractions run on TF32 tensor cores */
+    FA_DTYPE_BF16 = 1   /* bf16 in/out; fp32 accumulation and softmax */
+} fa_dtype_t;
+
+/*
+ * fa_fwd — enqueue the attention forward pass on `stream`.
+ *
+ *   q, k, v : device pointers, contiguous row-major [B, H, N, d] of `dtype`
+ *             (read only; they may alias one another).
+ *   o       : device pointer, [B, H, N, d] of `dtype`, written in full.
+ *   lse     : device pointer, fp32 [B, H, N], natural-log units; may be NULL,
+ *             which skips the store.
+ *   B, H, N : batch, heads, sequence length (queries = keys = N), each >= 1.
+ *   d       : head dimension: 64 or 128 for bf16, 64 for fp32.
+ *   scale   : finite score scale (1/sqrt(d) for the pages' attention).
+ *   dtype   : an fa_dtype_t value.
+ *   stream  : a cudaStream_t (NULL = the legacy default stream) on the
+ *             current device; all pointers must be on that device.
+ *
+ * Ownership: the caller owns every buffer; the library allocates and frees
+ * nothing on the device.  o and lse must not overlap the inputs or each other.
+ *
+ * Errors: argument checks run on the host before any CUDA call and return
+ * FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED / FA_ERR_ALIGNMENT without side
+ * effects.  A failed launch returns FA_ERR_CUDA.  The call is asynchronous:
+ * FA_OK means the kernel was enqueued; a kernel that aborted on a barrier
+ * timeout is reported by fa_device_status().  There is no CPU fallback.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int64_t B, int64_t H, int64_t N, int64_t d, float scale, int dtype,
+           void* stream);
+
+/*
+ * fa_fwd_validate — the host-side argument checks of fa_fwd, alone.  Returns
+ * the status fa_fwd would return before touching CUDA.  Makes no CUDA call,
+ * so it also runs on machines without a GPU.
+ */
+int fa_fwd_validate(const void* q, const void* k, const void* v, void* o,
+                    const float* lse, int64_t B, int64_t H, int64_t N,
+                    int64_t d, float scale, int dtype);
+
+/*
+ * fa_device_status — synchronise `stream`, then read and clear the device
+ * error word the kernels set when a bounded wait gives up.  Returns FA_OK,
+ * FA_ERR_TIMEOUT, or FA_ERR_CUDA if the synchronisation itself failed.
+ */
+int fa_device_status(void* stream);
+
+/* Static English text for a status code; never NULL. */
+const char* fa_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread's calls ("" if none). */
+const char* fa_last_error_message(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

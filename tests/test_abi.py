@@ -1,0 +1,100 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds for
+sm_103a, loads, exports every function include/fa.h declares, and its
+argument validation returns the documented status codes before any CUDA
+call."""
+import ctypes
+import math
+import subprocess
+
+import pytest
+
+from exact_tiled_attention_04_gb300 import binding as fab
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_tiled_attention_04_gb300 import build
+    build.build()
+    return fab.load()
+
+
+def test_header_declares_expected_entry_points():
+    names = fab.header_functions()
+    for n in ("fa_fwd", "fa_fwd_validate", "fa_device_status", "fa_status_string",
+              "fa_last_error_message", "fa_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", fab.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in fab.header_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings(lib):
+    for st in range(6):
+        assert fab.fa_status_string(st)
+    assert fab.fa_status_string(99) == "unknown status"
+    assert fab.fa_version() >= 100
+
+
+# fake, aligned, non-overlapping device addresses: validation never dereferences
+Q, K, V, O, L = 1 << 32, 2 << 32, 3 << 32, 4 << 32, 5 << 32
+GOOD = dict(B=2, H=4, N=1000, d=64, scale=0.125, dtype=fab.FA_DTYPE_BF16)
+
+
+def validate(q=Q, k=K, v=V, o=O, lse=L, **kw):
+    a = dict(GOOD)
+    a.update(kw)
+    return fab.fa_fwd_validate(q, k, v, o, lse, a["B"], a["H"], a["N"], a["d"], a["scale"], a["dtype"])
+
+
+def test_valid_arguments(lib):
+    assert validate() == fab.FA_OK
+    assert validate(lse=None) == fab.FA_OK
+    assert validate(d=128) == fab.FA_OK
+    assert validate(dtype=fab.FA_DTYPE_F32) == fab.FA_OK
+    assert validate(scale=0.0) == fab.FA_OK and validate(scale=-3.0) == fab.FA_OK
+    # inputs may alias one another
+    assert validate(k=Q, v=Q) == fab.FA_OK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), fab.FA_ERR_INVALID_ARG),
+    (dict(k=None), fab.FA_ERR_INVALID_ARG),
+    (dict(v=None), fab.FA_ERR_INVALID_ARG),
+    (dict(o=None), fab.FA_ERR_INVALID_ARG),
+    (dict(B=0), fab.FA_ERR_INVALID_ARG),
+    (dict(H=-1), fab.FA_ERR_INVALID_ARG),
+    (dict(N=0), fab.FA_ERR_INVALID_ARG),
+    (dict(scale=math.inf), fab.FA_ERR_INVALID_ARG),
+    (dict(scale=math.nan), fab.FA_ERR_INVALID_ARG),
+    (dict(d=96), fab.FA_ERR_UNSUPPORTED),
+    (dict(d=128, dtype=fab.FA_DTYPE_F32), fab.FA_ERR_UNSUPPORTED),
+    (dict(dtype=7), fab.FA_ERR_UNSUPPORTED),
+    (dict(q=Q + 8), fab.FA_ERR_ALIGNMENT),
+    (dict(o=O + 4), fab.FA_ERR_ALIGNMENT),
+    (dict(lse=L + 2), fab.FA_ERR_ALIGNMENT),
+    (dict(o=Q + 1024), fab.FA_ERR_INVALID_ARG),      # output overlaps an input
+    (dict(lse=O + 4096), fab.FA_ERR_INVALID_ARG),    # lse overlaps the output
+    (dict(B=1 << 40, H=1 << 30), fab.FA_ERR_INVALID_ARG),  # element count overflows
+    (dict(H=1 << 31, B=1), fab.FA_ERR_UNSUPPORTED),  # beyond 32-bit TMA coordinates
+])
+def test_invalid_arguments(lib, kw, status):
+    assert validate(**kw) == status
+
+
+def test_fa_fwd_rejects_bad_arguments_without_cuda(lib):
+    # same checks, same codes, and no CUDA call is made (this machine may
+    # have no GPU at all)
+    assert fab.fa_fwd(Q, K, V, O, L, 2, 4, 1000, 96, 0.125, fab.FA_DTYPE_BF16, None) == fab.FA_ERR_UNSUPPORTED
+    assert fab.fa_fwd(None, K, V, O, L, 2, 4, 1000, 64, 0.125, fab.FA_DTYPE_BF16, None) == fab.FA_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(fab, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        fab.load(str(tmp_path / "absent.so"))

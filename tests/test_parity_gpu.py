@@ -1,0 +1,136 @@
+"""Parity of the sm_103a forward kernel with the fp64 CPU oracle, called
+through the C ABI on seeded inputs.
+
+Tolerances (absolute, vs the fp64 oracle): O <= 1.5e-2 for bf16 in/out
+(fp32 accumulation), O <= 2e-3 for fp32 in/out (TF32 tensor cores),
+lse <= 1e-3.  Outputs are poisoned with NaN before each call so an unwritten
+element fails the comparison.
+"""
+import numpy as np
+import pytest
+
+from exact_tiled_attention_04_gb300 import inputs as I
+
+from .gpu_util import TOL_LSE, compare, edge_rows, ensure_library, run_fa, tol_o
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return ensure_library()
+
+
+def check(w, q, k, v, rows=None, scale=None):
+    o, lse = run_fa(w, q, k, v, scale=scale)
+    assert np.isfinite(o).all(), "unwritten or non-finite output"
+    assert np.isfinite(lse[..., :]).all(), "unwritten or non-finite lse"
+    err_o, err_l = compare(w, o, lse, q, k, v, rows=rows, scale=scale)
+    assert err_o <= tol_o(w), (w.describe(), err_o)
+    assert err_l <= TOL_LSE, (w.describe(), err_l)
+    return o, lse, err_o, err_l
+
+
+@pytest.mark.parametrize("name", ["single_head_n512", "tail_n1000", "b4h16_n2048"])
+def test_workload_every_row(name):
+    w = I.WORKLOADS[name]
+    q, k, v = I.make(w)
+    check(w, q, k, v)
+
+
+@pytest.mark.parametrize("name", ["b2h32_n8192_d128", "long_n16384"])
+def test_workload_sampled_rows(name):
+    w = I.WORKLOADS[name]
+    q, k, v = I.make(w)
+    check(w, q, k, v, rows=edge_rows(w, w.oracle_rows))
+
+
+def test_tail_workload_special_heads():
+    """Identical keys: exactly the mean of the 1000 V rows (tail keys masked,
+    not averaged in); Q x30: within tolerance of the oracle's near one-hot
+    rows."""
+    w = I.WORKLOADS["tail_n1000"]
+    q, k, v = I.make(w)
+    o, lse = run_fa(w, q, k, v)
+    mean_v = v[0, 1].astype(np.float64).mean(axis=0)
+    assert np.max(np.abs(o[0, 1] - mean_v)) <= tol_o(w)
+    s0 = float(w.scale) * float(q[0, 1, 0].astype(np.float64) @ k[0, 1, 0].astype(np.float64))
+    assert abs(lse[0, 1, 0] - (s0 + np.log(w.N))) <= TOL_LSE
+    err_o, err_l = compare(w, o, lse, q, k, v, rows=[(1, 2, i) for i in range(w.N)])
+    assert err_o <= tol_o(w) and err_l <= TOL_LSE
+
+
+@pytest.mark.parametrize("N", [1, 2, 63, 127, 128, 129, 255, 256, 257, 383, 640])
+@pytest.mark.parametrize("d", [64, 128])
+def test_edge_lengths_bf16(N, d):
+    w = I.custom(1, 2, N, d, "bf16", seed=100 + N)
+    q, k, v = I.make(w)
+    check(w, q, k, v)
+
+
+@pytest.mark.parametrize("N", [1, 100, 129, 256, 700])
+def test_edge_lengths_f32(N):
+    w = I.custom(1, 2, N, 64, "f32", seed=200 + N)
+    q, k, v = I.make(w)
+    check(w, q, k, v)
+
+
+def test_more_heads_than_sms():
+    w = I.custom(2, 160, 256, 64, "bf16", seed=7)
+    q, k, v = I.make(w)
+    check(w, q, k, v, rows=edge_rows(w, 512))
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.2, 0.9])
+def test_scale_values(scale):
+    w = I.custom(1, 2, 300, 64, "bf16", seed=8)
+    q, k, v = I.make(w)
+    o, lse, _, _ = check(w, q, k, v, scale=np.float32(scale))
+    if scale == 0.0:
+        assert np.max(np.abs(o - v.astype(np.float64).mean(axis=2, keepdims=True))) <= tol_o(w)
+        assert np.max(np.abs(lse - np.log(w.N))) <= TOL_LSE
+
+
+def test_lse_optional_and_deterministic():
+    w = I.custom(2, 3, 777, 128, "bf16", seed=9)
+    q, k, v = I.make(w)
+    o1, l1 = run_fa(w, q, k, v)
+    o2, l2 = run_fa(w, q, k, v)
+    o3, l3 = run_fa(w, q, k, v, with_lse=False)
+    assert l3 is None
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2) and np.array_equal(o1, o3)
+
+
+def test_inputs_unchanged_and_side_stream():
+    from exact_tiled_attention_04_gb300 import binding as fab
+    from .gpu_util import to_device
+    w = I.custom(1, 4, 513, 64, "bf16", seed=10)
+    q, k, v = I.make(w)
+    tq, tk, tv = (to_device(x, w.dtype) for x in (q, k, v))
+    before = [t.clone() for t in (tq, tk, tv)]
+    o = torch.empty_like(tq)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    torch.cuda.current_stream().synchronize()
+    st = fab.fa_fwd(tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                    w.B, w.H, w.N, w.d, float(w.scale), fab.FA_DTYPE_BF16, s.cuda_stream)
+    assert st == 0
+    assert fab.fa_device_status(s.cuda_stream) == 0
+    for a, b in zip(before, (tq, tk, tv)):
+        assert torch.equal(a, b)
+    err_o, err_l = compare(w, o.float().cpu().numpy(), lse.cpu().numpy(), q, k, v)
+    assert err_o <= tol_o(w) and err_l <= TOL_LSE
+
+
+def test_torch_convenience_wrapper():
+    import exact_tiled_attention_04_gb300 as fa
+    w = I.custom(1, 2, 200, 128, "bf16", seed=12)
+    q, k, v = I.make(w)
+    from .gpu_util import to_device
+    out, lse = fa.attention(*(to_device(x, "bf16") for x in (q, k, v)))
+    torch.cuda.synchronize()
+    err_o, err_l = compare(w, out.float().cpu().numpy(), lse.cpu().numpy(), q, k, v)
+    assert err_o <= tol_o(w) and err_l <= TOL_LSE
