@@ -11,4 +11,5 @@ was not built.
 from .binding import (FA_DTYPE_BF16, FA_DTYPE_F32, FA_ERR_ALIGNMENT, FA_ERR_CUDA,  # noqa: F401
                       FA_ERR_INVALID_ARG, FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED, FA_OK, FAError,
                       attention, fa_device_status, fa_fwd, fa_fwd_validate,
-                      fa_last_error_message, fa_status_string, fa_version)
+                      fa_last_error_message, fa_selftest_barrier_timeout, fa_status_string,
+                      fa_version)

@@ -73,6 +73,8 @@ def load(path: str | None = None):
         lib.fa_last_error_message.argtypes = []
         lib.fa_version.restype = c_int
         lib.fa_version.argtypes = []
+        lib.fa_selftest_barrier_timeout.restype = c_int
+        lib.fa_selftest_barrier_timeout.argtypes = [vp]
         _lib = lib
         return lib
 
@@ -98,6 +100,10 @@ def fa_fwd_validate(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: 
 
 def fa_device_status(stream: int | None) -> int:
     return load().fa_device_status(stream or None)
+
+
+def fa_selftest_barrier_timeout(stream: int | None) -> int:
+    return load().fa_selftest_barrier_timeout(stream or None)
 
 
 def fa_status_string(status: int) -> str:

@@ -9,8 +9,10 @@
 // dimension checked instead of assumed), extended with batch, heads, dtype,
 // the log-sum-exp output and a stream.
 #include <cmath>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -18,8 +20,8 @@
 #include "fa.h"
 #include "fa_internal.h"
 
-// Set by the kernels when a bounded wait gives up (one word per device).
-__device__ unsigned int g_fa_device_error;
+// Set by the kernels when a bounded wait gives up (one per device).
+__device__ fa::DevStatus g_fa_device_status;
 
 namespace {
 
@@ -47,11 +49,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 constexpr int kMaxDevices = 64;
-unsigned int* g_err_ptr[kMaxDevices] = {};
+fa::DevStatus* g_err_ptr[kMaxDevices] = {};
 std::mutex g_err_mutex;
+std::atomic<unsigned int> g_generation{0};
 
-// Device address of the error word on the current device.
-unsigned int* device_error_word(int* status) {
+// Launch generation: never 0 (0 is the status word's initial abort_gen).
+unsigned int next_generation() {
+    unsigned int g = ++g_generation;
+    if (g == 0) g = ++g_generation;
+    return g;
+}
+
+// Device address of the status words on the current device.
+fa::DevStatus* device_status_words(int* status) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -62,13 +72,13 @@ unsigned int* device_error_word(int* status) {
     std::lock_guard<std::mutex> lock(g_err_mutex);
     if (g_err_ptr[dev] == nullptr) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_fa_device_error);
+        e = cudaGetSymbolAddress(&p, g_fa_device_status);
         if (e != cudaSuccess) {
             set_error("cudaGetSymbolAddress", static_cast<int>(e), cudaGetErrorString(e));
             *status = FA_ERR_CUDA;
             return nullptr;
         }
-        g_err_ptr[dev] = static_cast<unsigned int*>(p);
+        g_err_ptr[dev] = static_cast<fa::DevStatus*>(p);
     }
     *status = FA_OK;
     return g_err_ptr[dev];
@@ -178,8 +188,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 
     fa::FwdParams p;
     p.lse = lse;
-    p.err = device_error_word(&st);
+    p.status = device_status_words(&st);
     if (st != FA_OK) return st;
+    p.gen = next_generation();
     p.N = static_cast<int>(N);
     p.n_kv_tiles = static_cast<int>((N + 127) / 128);
     p.n_q_blocks = static_cast<int>((N + 255) / 256);
@@ -207,21 +218,35 @@ int fa_device_status(void* stream) {
         set_error("cudaStreamSynchronize", static_cast<int>(e), cudaGetErrorString(e));
         return FA_ERR_CUDA;
     }
-    unsigned int word = 0;
-    e = cudaMemcpyFromSymbol(&word, g_fa_device_error, sizeof(word));
+    fa::DevStatus st{};
+    e = cudaMemcpyFromSymbol(&st, g_fa_device_status, sizeof(st));
     if (e != cudaSuccess) {
         set_error("cudaMemcpyFromSymbol", static_cast<int>(e), cudaGetErrorString(e));
         return FA_ERR_CUDA;
     }
-    if (word == 0) return FA_OK;
+    if (st.word == 0) return FA_OK;
     const unsigned int zero = 0;
-    e = cudaMemcpyToSymbol(g_fa_device_error, &zero, sizeof(zero));
+    e = cudaMemcpyToSymbol(g_fa_device_status, &zero, sizeof(zero), offsetof(fa::DevStatus, word));
     if (e != cudaSuccess) {
         set_error("cudaMemcpyToSymbol", static_cast<int>(e), cudaGetErrorString(e));
         return FA_ERR_CUDA;
     }
-    std::snprintf(g_last_error, sizeof(g_last_error), "device error word 0x%08x", word);
-    return (word & fa::kDevErrTimeout) ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
+    std::snprintf(g_last_error, sizeof(g_last_error), "device error word 0x%08x", st.word);
+    return (st.word & fa::kDevErrTimeout) ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
+}
+
+int fa_selftest_barrier_timeout(void* stream) {
+    int st = FA_OK;
+    fa::FwdParams p{};
+    p.status = device_status_words(&st);
+    if (st != FA_OK) return st;
+    p.gen = next_generation();
+    cudaError_t e = fa::launch_selftest_wait(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        set_error("fa_selftest_barrier_timeout launch", static_cast<int>(e), cudaGetErrorString(e));
+        return FA_ERR_CUDA;
+    }
+    return FA_OK;
 }
 
 }  // extern "C"

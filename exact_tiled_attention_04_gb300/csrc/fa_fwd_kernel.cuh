@@ -11,11 +11,13 @@
 // Shared Memory Tiling", Kernel 2).  The N x N score matrix never leaves the
 // SM.
 //
-// Organisation (one CTA = 256 query rows of one (batch, head), 320 threads):
+// Organisation (one CTA = 256 query rows of one (batch, head), 384 threads):
 //   warps 0-3  softmax warpgroup 0: query tile 0 (rows 0-127 of the block)
 //   warps 4-7  softmax warpgroup 1: query tile 1 (rows 128-255)
-//   warp  8    tensor-core issuer (one thread) and TMEM owner
-//   warp  9    TMA producer (one thread)
+//   warp  8    tensor-core issuer of tile 0 (one thread) and TMEM owner
+//   warp  9    TMA producer (one thread; the whole warp for fp32 inputs)
+//   warp 10    tensor-core issuer of tile 1 (one thread)
+//   warp 11    idle (completes warpgroup 2 for the register reallocation)
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   S_w  columns [128w, 128w+128)   scores of tile w; P_w overwrites its
 //                                   first columns (bf16 pairs or tf32)
@@ -23,11 +25,12 @@
 // Shared memory (128-byte-swizzled TMA tiles, 1024-byte aligned):
 //   Q_0, Q_1 (reused as the output staging tiles), a ring of K tiles and a
 //   ring of V tiles, then the mbarriers.
-// Tensor-core schedule per key tile j (w = 0, 1 alternate, so the softmax of
-// one tile overlaps the matrix products of the other):
-//   S_0(j) = Q_0 K_j^T   S_1(j) = Q_1 K_j^T   O_0 += P_0(j) V_j
-//   S_0(j+1)             O_1 += P_1(j) V_j    S_1(j+1) ...
-//
+// Tensor-core work per key tile j and tile w, enqueued by tile w's issuer:
+//   O_w += P_w(j) V_j as soon as P_w(j) is ready, then S_w(j+1) = Q_w K_{j+1}^T
+//   (which overwrites P_w(j) in TMEM: same thread, so the tensor core runs
+//   them in order).  While one tile's softmax runs, the other tile's
+//   products keep the tensor core busy.
+
 // Online-softmax details:
 //   * scores are handled in base 2: t = s * scale * log2(e), p = 2^(t - m);
 //   * the reference maximum m is only moved when the tile maximum exceeds
@@ -58,16 +61,14 @@ constexpr int kTileM = 128;  // query rows per softmax warpgroup = TMEM lanes
 constexpr int kTileN = 128;  // keys per K/V tile
 // Three warpgroups: two softmax warpgroups and one holding the tensor-core
 // issuer warp, the TMA warp and two idle warps.  Registers are allocated per
-// warpgroup, so the launch gets 384 x 168; setmaxnreg then moves them to
-// the softmax warpgroups (2 x 128 x 216 + 128 x 72 = 384 x 168).
+// warpgroup, so the launch gets 384 x 168; setmaxnreg then moves them from
+// warpgroup 2 to the softmax warpgroups (per variant, see FwdCfg: the split
+// always sums to 384 x 168).
 constexpr int kThreads = 384;
-constexpr int kMmaWarp = 8;
+constexpr int kMmaWarp = 8;   // tensor-core issuer of query tile 0, TMEM owner
+constexpr int kMmaWarp2 = 10; // tensor-core issuer of query tile 1
 constexpr int kLoadWarp = 9;
 constexpr uint32_t kLaunchRegs = 168;
-constexpr uint32_t kSoftmaxRegs = 216;
-constexpr uint32_t kOtherRegs = 72;
-static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs == kThreads * kLaunchRegs,
-              "register split must equal the launch allocation");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
@@ -100,6 +101,13 @@ struct FwdCfg {
     static constexpr int kPvSplit = 1;
     static constexpr uint32_t kIdescPV = instr_desc(kFmt, false, !TF32, kTileM, kPvN);
 
+    // register split (setmaxnreg): softmax warpgroups / warpgroup 2, chosen
+    // so that neither side spills
+    static constexpr uint32_t kSoftmaxRegs = TF32 ? 200 : 208;
+    static constexpr uint32_t kOtherRegs = TF32 ? 104 : 88;
+    static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs == kThreads * kLaunchRegs,
+                  "register split must equal the launch allocation");
+
     // shared-memory map (offsets from the 1024-aligned base)
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + 2 * kTileBytes;
@@ -113,14 +121,15 @@ struct FwdCfg {
     static constexpr int kBarVFull = kBarKEmpty + kKStages;
     static constexpr int kBarVEmpty = kBarVFull + kVStages;
     static constexpr int kBarSFull = kBarVEmpty + kVStages;  // [2]
-    static constexpr int kBarPFull = kBarSFull + 2;          // [2]
-    static constexpr int kBarOFull = kBarPFull + 2;          // [2]
+    static constexpr int kBarPFull = kBarSFull + 2;          // [2 tiles][2 halves]
+    static constexpr int kBarOFull = kBarPFull + 4;          // [2]
     static constexpr int kBarEpi = kBarOFull + 2;            // [2]
-    static constexpr int kBarDrain = kBarEpi + 2;
-    static constexpr int kBarQRaw = kBarDrain + 1;  // fp32 only: TMA landed, not yet rounded
+    static constexpr int kBarDrain = kBarEpi + 2;            // [2]
+    static constexpr int kBarQRaw = kBarDrain + 2;  // fp32 only: TMA landed, not yet rounded
     static constexpr int kBarKRaw = kBarQRaw + 1;   // [kKStages]
     static constexpr int kBarVRaw = kBarKRaw + kKStages;
-    static constexpr int kNumBars = kBarVRaw + 1;
+    static constexpr int kBarTurn = kBarVRaw + 1;  // [2]: softmax warpgroup w may start a tile
+    static constexpr int kNumBars = kBarTurn + 2;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kSmemUsed = kOffAbort + 4;
@@ -132,9 +141,17 @@ struct FwdCfg {
 // Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting
 // (if `honor_abort`) or when this wait itself gave up after kWaitLimitNs, in
 // which case it raises the abort flag and the device error word.
+// Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting
+// (if `honor_abort`) or when this wait itself gave up after kWaitLimitNs, in
+// which case it raises the CTA's abort flag, sets the sticky device error
+// bits (with the waiting role in bits 8-15) and marks this launch's
+// generation as aborted, so CTAs of the same launch that start later skip
+// their work.  Later launches are not affected.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
-                                           volatile uint32_t* abort_flag, unsigned int* err,
+                                           volatile uint32_t* abort_flag, const FwdParams& fp,
                                            unsigned int where, bool honor_abort = true) {
+    DevStatus* const status = fp.status;
+    const unsigned int gen = fp.gen;
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     uint32_t spins = 0;
@@ -144,7 +161,8 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
             if (honor_abort && *abort_flag) return false;
             if (global_timer_ns() - t0 > kWaitLimitNs) {
                 *abort_flag = 1u;
-                atomicOr(err, kDevErrTimeout | (where << 8));
+                atomicOr(&status->word, kDevErrTimeout | (where << 8));
+                atomicExch(&status->abort_gen, gen);
                 return false;
             }
         }
@@ -172,22 +190,19 @@ __device__ __forceinline__ float row_extreme(const uint32_t (&s)[4][32]) {
     return two(three(acc[0], acc[1], acc[2]), three(acc[3], acc[4], two(acc[5], three(acc[6], acc[7], acc[7]))));
 }
 
-// Softmax numerators of one 128-key score row held in registers:
-// p_j = 2^(s_j * c - shift), keys >= `valid` get p = 0 (kMasked, last tile
-// only).  Writes P into tensor memory at `tS` (bf16 pairs, or TF32 values one
-// per column) and adds sum p (fp32) to l and the sum of the rounded p, the
-// weights the P V product actually uses, to lq.  Pairs of keys go through the
-// packed f32x2 FMA / add; eight independent partial sums.
+// Softmax numerators of one half (keys 64h .. 64h+63) of a 128-key score row
+// held in registers: p_j = 2^(s_j * c - shift), keys >= `valid` get p = 0
+// (kMasked, last tile only).  Writes P into tensor memory over the scores
+// (bf16 pairs in 32 columns, or TF32 values in 64 columns) and adds p (fp32)
+// into acc, per packed lane pair.  Pairs of keys go through the packed
+// f32x2 FMA / add.
 template <bool TF32, bool kMasked>
-__device__ __forceinline__ void exp_tile(const uint32_t (&s)[4][32], float c, float shift, int valid,
-                                         uint32_t tS, float& l, float& lq) {
-    const uint64_t c2 = f2_pack(c, c);
-    const uint64_t ns2 = f2_pack(-shift, -shift);
-    uint64_t acc[4] = {0, 0, 0, 0};
-    uint64_t qacc[4] = {0, 0, 0, 0};
+__device__ __forceinline__ void exp_half(const uint32_t (&s)[4][32], uint64_t c2, uint64_t ns2,
+                                         int valid, uint32_t tS, int h, uint64_t (&acc)[4]) {
     if constexpr (TF32) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int qq = 0; qq < 2; ++qq) {
+            const int q = 2 * h + qq;
             uint32_t pw[32];
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
@@ -201,41 +216,36 @@ __device__ __forceinline__ void exp_tile(const uint32_t (&s)[4][32], float c, fl
                 pw[i] = round_tf32(p0);
                 pw[i + 1] = round_tf32(p1);
                 acc[(i / 2) & 3] = f2_add(acc[(i / 2) & 3], f2_pack(p0, p1));
-                qacc[(i / 2) & 3] = f2_add(qacc[(i / 2) & 3], f2_pack(u2f(pw[i]), u2f(pw[i + 1])));
             }
             tmem_st32(tS + 32u * q, pw);
         }
     } else {
+        uint32_t pw[32];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t pw[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int c0 = h * 64 + 2 * i;  // keys c0, c0 + 1
-                float t0, t1;
-                f2_unpack(f2_fma(f2_pack(u2f(s[c0 / 32][c0 % 32]), u2f(s[c0 / 32][c0 % 32 + 1])), c2, ns2),
-                          t0, t1);
-                float p0 = ex2(t0), p1 = ex2(t1);
-                if constexpr (kMasked) {
-                    if (c0 >= valid) p0 = 0.0f;
-                    if (c0 + 1 >= valid) p1 = 0.0f;
-                }
-                const uint32_t pk = pack_bf16x2(p0, p1);
-                pw[i] = pk;
-                acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-                qacc[i & 3] = f2_add(qacc[i & 3], f2_pack(u2f(pk << 16), u2f(pk & 0xFFFF0000u)));
+        for (int i = 0; i < 32; ++i) {
+            const int c0 = h * 64 + 2 * i;  // keys c0, c0 + 1
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(u2f(s[c0 / 32][c0 % 32]), u2f(s[c0 / 32][c0 % 32 + 1])), c2, ns2),
+                      t0, t1);
+            float p0 = ex2(t0), p1 = ex2(t1);
+            if constexpr (kMasked) {
+                if (c0 >= valid) p0 = 0.0f;
+                if (c0 + 1 >= valid) p1 = 0.0f;
             }
-            tmem_st32(tS + 32u * h, pw);
+            const uint32_t pk = pack_bf16x2(p0, p1);
+            pw[i] = pk;
+            acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
         }
+        tmem_st32(tS + 32u * h, pw);
     }
-    float a[8], b[8];
+}
+
+// Sum of the eight fp32 lanes of four packed pairs.
+__device__ __forceinline__ float sum8(const uint64_t (&a)[4]) {
+    float x[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        f2_unpack(acc[k], a[2 * k], a[2 * k + 1]);
-        f2_unpack(qacc[k], b[2 * k], b[2 * k + 1]);
-    }
-    l += ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
-    lq += ((b[0] + b[1]) + (b[2] + b[3])) + ((b[4] + b[5]) + (b[6] + b[7]));
+    for (int k = 0; k < 4; ++k) f2_unpack(a[k], x[2 * k], x[2 * k + 1]);
+    return ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
 }
 
 // Round `n16` 16-byte groups of fp32 in shared memory to TF32 in place
@@ -302,7 +312,7 @@ __device__ void produce_tf32(const CUtensorMap& map_q, const CUtensorMap& map_k,
                             bar(C::kBarQRaw), a * C::kAtomElems, row0 + w * kTileM, bh, once);
     }
     q_issued = true;
-    ok = all_ok(wait_phase(bar(C::kBarQRaw), 0, abort_flag, p.err, 20));
+    ok = all_ok(wait_phase(bar(C::kBarQRaw), 0, abort_flag, p, 20));
     if (ok) {
         round_tf32_inplace(smem + C::kOffQ, 2 * C::kTileBytes / 16, lane);
         fence_proxy_async_smem();
@@ -312,7 +322,7 @@ __device__ void produce_tf32(const CUtensorMap& map_q, const CUtensorMap& map_k,
     for (int j = 0; ok && j < T; ++j) {
         const int ks = j % C::kKStages;
         const int vs = j % C::kVStages;
-        ok = all_ok(wait_phase(bar(C::kBarKEmpty + ks), ((j / C::kKStages) & 1) ^ 1, abort_flag, p.err, 21));
+        ok = all_ok(wait_phase(bar(C::kBarKEmpty + ks), ((j / C::kKStages) & 1) ^ 1, abort_flag, p, 21));
         if (!ok) break;
         if (lane == 0) {
             mbar_arrive_expect_tx(bar(C::kBarKRaw + ks), C::kTileBytes);
@@ -327,15 +337,15 @@ __device__ void produce_tf32(const CUtensorMap& map_q, const CUtensorMap& map_k,
         }
         nk = j + 1;
         nv = j + 1;
-        ok = all_ok(wait_phase(bar(C::kBarKRaw + ks), (j / C::kKStages) & 1, abort_flag, p.err, 22));
+        ok = all_ok(wait_phase(bar(C::kBarKRaw + ks), (j / C::kKStages) & 1, abort_flag, p, 22));
         if (!ok) break;
         round_tf32_inplace(smem + C::kOffK + ks * C::kTileBytes, C::kTileBytes / 16, lane);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::kBarKFull + ks));
-        ok = all_ok(wait_phase(bar(C::kBarVRaw), j & 1, abort_flag, p.err, 23));
+        ok = all_ok(wait_phase(bar(C::kBarVRaw), j & 1, abort_flag, p, 23));
         if (!ok) break;
-        ok = all_ok(wait_phase(bar(C::kBarVEmpty + vs), ((j / C::kVStages) & 1) ^ 1, abort_flag, p.err, 24));
+        ok = all_ok(wait_phase(bar(C::kBarVEmpty + vs), ((j / C::kVStages) & 1) ^ 1, abort_flag, p, 24));
         if (!ok) break;
         transpose_v_tf32<D>(smem + C::kOffVRaw, smem + C::kOffV + vs * C::kTileBytes, lane);
         fence_proxy_async_smem();
@@ -344,12 +354,12 @@ __device__ void produce_tf32(const CUtensorMap& map_q, const CUtensorMap& map_k,
     }
     // Drain every TMA load this warp issued (see the bf16 producer).
     if (lane == 0) {
-        if (q_issued) wait_phase(bar(C::kBarQRaw), 0, abort_flag, p.err, 25, false);
+        if (q_issued) wait_phase(bar(C::kBarQRaw), 0, abort_flag, p, 25, false);
         for (int s = 0; s < C::kKStages && s < nk; ++s) {
             const int last = s + ((nk - 1 - s) / C::kKStages) * C::kKStages;
-            wait_phase(bar(C::kBarKRaw + s), (last / C::kKStages) & 1, abort_flag, p.err, 25, false);
+            wait_phase(bar(C::kBarKRaw + s), (last / C::kKStages) & 1, abort_flag, p, 25, false);
         }
-        if (nv > 0) wait_phase(bar(C::kBarVRaw), (nv - 1) & 1, abort_flag, p.err, 25, false);
+        if (nv > 0) wait_phase(bar(C::kBarVRaw), (nv - 1) & 1, abort_flag, p, 25, false);
     }
 }
 
@@ -381,24 +391,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(C::kBarQFull), 1);
         for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(bar(C::kBarKFull + s), 1);
-            mbar_init(bar(C::kBarKEmpty + s), 1);
+            mbar_init(bar(C::kBarKEmpty + s), 2);  // both issuers' commits
         }
         for (int s = 0; s < C::kVStages; ++s) {
             mbar_init(bar(C::kBarVFull + s), 1);
-            mbar_init(bar(C::kBarVEmpty + s), 1);
+            mbar_init(bar(C::kBarVEmpty + s), 2);
         }
         for (int w = 0; w < 2; ++w) {
             mbar_init(bar(C::kBarSFull + w), 1);
-            mbar_init(bar(C::kBarPFull + w), 4);  // one arrival per softmax warp
+            mbar_init(bar(C::kBarPFull + 2 * w + 0), 4);  // one arrival per softmax warp
+            mbar_init(bar(C::kBarPFull + 2 * w + 1), 4);
+            mbar_init(bar(C::kBarTurn + w), 4);
             mbar_init(bar(C::kBarOFull + w), 1);
             mbar_init(bar(C::kBarEpi + w), kTileM);
         }
-        mbar_init(bar(C::kBarDrain), 1);
+        mbar_init(bar(C::kBarDrain + 0), 1);
+        mbar_init(bar(C::kBarDrain + 1), 1);
         mbar_init(bar(C::kBarQRaw), 1);
         for (int s = 0; s < C::kKStages; ++s) mbar_init(bar(C::kBarKRaw + s), 1);
         mbar_init(bar(C::kBarVRaw), 1);
-        // A CTA starting after another one timed out does no work.
-        *abort_flag = (*reinterpret_cast<volatile unsigned int*>(p.err) != 0u) ? 1u : 0u;
+        // A CTA starting after another CTA of this launch timed out does no work.
+        *abort_flag = (*reinterpret_cast<volatile unsigned int*>(&p.status->abort_gen) == p.gen) ? 1u : 0u;
         mbar_init_fence();
     }
     if (warp == kLoadWarp && lane == 0) {
@@ -420,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // nothing issued: go straight to the teardown
     } else if (warp >= 8) {
         // warpgroup 2: TMA producer, tensor-core issuer, two idle warps
-        regs_decrease<kOtherRegs>();
+        regs_decrease<C::kOtherRegs>();
       if (warp == kLoadWarp) {
         // ------------------------------------------------------ TMA producer
         if constexpr (TF32) {
@@ -436,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int nk = 0, nv = 0;  // K and V tiles whose loads were issued
             for (int j = 0; j < T; ++j) {
                 const int ks = j % C::kKStages;
-                if (!wait_phase(bar(C::kBarKEmpty + ks), ((j / C::kKStages) & 1) ^ 1, abort_flag, p.err, 1))
+                if (!wait_phase(bar(C::kBarKEmpty + ks), ((j / C::kKStages) & 1) ^ 1, abort_flag, p, 1))
                     break;
                 mbar_arrive_expect_tx(bar(C::kBarKFull + ks), C::kTileBytes);
                 for (int a = 0; a < C::kAtoms; ++a)
@@ -444,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 bar(C::kBarKFull + ks), a * C::kAtomElems, j * kTileN, bh, keep);
                 nk = j + 1;
                 const int vs = j % C::kVStages;
-                if (!wait_phase(bar(C::kBarVEmpty + vs), ((j / C::kVStages) & 1) ^ 1, abort_flag, p.err, 2))
+                if (!wait_phase(bar(C::kBarVEmpty + vs), ((j / C::kVStages) & 1) ^ 1, abort_flag, p, 2))
                     break;
                 mbar_arrive_expect_tx(bar(C::kBarVFull + vs), C::kTileBytes);
                 for (int a = 0; a < C::kAtoms; ++a)
@@ -457,22 +470,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             // path these phases completed long ago.  The last tile loaded
             // into stage s is the largest index below the issued count that
             // is congruent to s.
-            wait_phase(bar(C::kBarQFull), 0, abort_flag, p.err, 3, false);
+            wait_phase(bar(C::kBarQFull), 0, abort_flag, p, 3, false);
             for (int s = 0; s < C::kKStages && s < nk; ++s) {
                 const int last = s + ((nk - 1 - s) / C::kKStages) * C::kKStages;
-                wait_phase(bar(C::kBarKFull + s), (last / C::kKStages) & 1, abort_flag, p.err, 3, false);
+                wait_phase(bar(C::kBarKFull + s), (last / C::kKStages) & 1, abort_flag, p, 3, false);
             }
             for (int s = 0; s < C::kVStages && s < nv; ++s) {
                 const int last = s + ((nv - 1 - s) / C::kVStages) * C::kVStages;
-                wait_phase(bar(C::kBarVFull + s), (last / C::kVStages) & 1, abort_flag, p.err, 3, false);
+                wait_phase(bar(C::kBarVFull + s), (last / C::kVStages) & 1, abort_flag, p, 3, false);
             }
         }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------- tensor-core issuer
+    } else if (warp == kMmaWarp || warp == kMmaWarp2) {
+        // ------------------------------------------------ tensor-core issuers
+        // One issuing thread per query tile (warp 8: tile 0, warp 10: tile 1),
+        // so each tile's products are enqueued as soon as its P is ready,
+        // never behind the other tile's instructions.  Both read the same K/V
+        // stages; each stage is released when both issuers' products that
+        // read it have completed (empty barriers count two commits).
         if (lane == 0) {
-            auto issue_qk = [&](int w, int ks) {
-                const uint32_t dS = tmem + (w ? 128u : 0u);
-                const uint32_t sQ = sbase + C::kOffQ + (w ? C::kTileBytes : 0);
+            const int w = (warp == kMmaWarp) ? 0 : 1;
+            const uint32_t dS = tmem + 128u * static_cast<uint32_t>(w);
+            const uint32_t dO = tmem + 256u + static_cast<uint32_t>(D * w);
+            const uint32_t sQ = sbase + C::kOffQ + w * C::kTileBytes;
+            auto issue_qk = [&](int ks) {
                 const uint32_t sK = sbase + C::kOffK + ks * C::kTileBytes;
 #pragma unroll
                 for (int kk = 0; kk < C::kQkSteps; ++kk) {
@@ -482,12 +502,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ss<TF32>(dS, da, db, C::kIdescQK, kk > 0 ? 1u : 0u);
                 }
             };
-            auto issue_pv = [&](int w, int vs, bool accumulate) {
-                const uint32_t aP = tmem + (w ? 128u : 0u);
-                const uint32_t dO = tmem + 256u + (w ? static_cast<uint32_t>(D) : 0u);
+            // k-steps [k0, k1) of O_w += P_w V
+            auto issue_pv = [&](int vs, bool accumulate, int k0, int k1) {
                 const uint32_t sV = sbase + C::kOffV + vs * C::kTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < C::kPvSteps; ++kk) {
+                for (int kk = k0; kk < k1; ++kk) {
                     uint64_t db;
                     if constexpr (TF32) {
                         // V^T, K-major: 32-key atoms of D rows; a k-step is 8 keys (32 bytes)
@@ -497,60 +516,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // kAtomBytes apart; a k-step is 16 rows
                         db = smem_desc_sw128(sV + kk * C::kUmmaK * 128, C::kAtomBytes, 1024);
                     }
-                    mma_ts<TF32>(dO, aP + kk * 8, db, C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+                    mma_ts<TF32>(dO, dS + kk * 8, db, C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
                 }
             };
 
-            bool ok = wait_phase(bar(C::kBarQFull), 0, abort_flag, p.err, 4);
-            if (ok) ok = wait_phase(bar(C::kBarKFull + 0), 0, abort_flag, p.err, 4);
+            bool ok = wait_phase(bar(C::kBarQFull), 0, abort_flag, p, 4);
+            if (ok) ok = wait_phase(bar(C::kBarKFull + 0), 0, abort_flag, p, 4);
             if (ok) {
                 tc_fence_after();
-                issue_qk(0, 0);
-                tc_commit(bar(C::kBarSFull + 0));
-                issue_qk(1, 0);
-                tc_commit(bar(C::kBarSFull + 1));
+                issue_qk(0);
+                tc_commit(bar(C::kBarSFull + w));
                 tc_commit(bar(C::kBarKEmpty + 0));
             }
             for (int j = 0; ok && j < T; ++j) {
                 const int vs = j % C::kVStages;
                 const int ks = (j + 1) % C::kKStages;
-                ok = wait_phase(bar(C::kBarVFull + vs), (j / C::kVStages) & 1, abort_flag, p.err, 5);
+                ok = wait_phase(bar(C::kBarVFull + vs), (j / C::kVStages) & 1, abort_flag, p, 5);
                 if (!ok) break;
-                ok = wait_phase(bar(C::kBarPFull + 0), j & 1, abort_flag, p.err, 6);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv(0, vs, j > 0);
-                if (j + 1 < T) {
-                    ok = wait_phase(bar(C::kBarKFull + ks), ((j + 1) / C::kKStages) & 1, abort_flag, p.err, 7);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_qk(0, ks);
-                    tc_commit(bar(C::kBarSFull + 0));
-                } else {
-                    tc_commit(bar(C::kBarOFull + 0));
-                }
-                ok = wait_phase(bar(C::kBarPFull + 1), j & 1, abort_flag, p.err, 8);
+                // the first half of P (keys 0-63) is published before the
+                // second, so its products start while the softmax finishes
+                ok = wait_phase(bar(C::kBarPFull + 2 * w), j & 1, abort_flag, p, 6);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(1, vs, j > 0);
+                issue_pv(vs, j > 0, 0, C::kPvSteps / 2);
+                ok = wait_phase(bar(C::kBarPFull + 2 * w + 1), j & 1, abort_flag, p, 6);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(vs, true, C::kPvSteps / 2, C::kPvSteps);
                 tc_commit(bar(C::kBarVEmpty + vs));
                 if (j + 1 < T) {
-                    issue_qk(1, ks);
-                    tc_commit(bar(C::kBarSFull + 1));
+                    ok = wait_phase(bar(C::kBarKFull + ks), ((j + 1) / C::kKStages) & 1, abort_flag, p, 7);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_qk(ks);
+                    tc_commit(bar(C::kBarSFull + w));
                     tc_commit(bar(C::kBarKEmpty + ks));
                 } else {
-                    tc_commit(bar(C::kBarOFull + 1));
+                    tc_commit(bar(C::kBarOFull + w));
                 }
             }
-            // Drain every tensor-core operation issued so far before the
+            // Drain every tensor-core operation this thread issued before the
             // tensor memory is released.
-            tc_commit(bar(C::kBarDrain));
-            wait_phase(bar(C::kBarDrain), 0, abort_flag, p.err, 9, false);
+            tc_commit(bar(C::kBarDrain + w));
+            wait_phase(bar(C::kBarDrain + w), 0, abort_flag, p, 9, false);
         }
       }
     } else {
         // ------------------------------------------------ softmax warpgroups
-        regs_increase<kSoftmaxRegs>();
+        regs_increase<C::kSoftmaxRegs>();
         const int w = warp / 4;   // query tile of this warpgroup
         const int wi = warp % 4;  // TMEM lane quarter this warp may access
         const int t = wi * 32 + lane;  // row within the tile = TMEM lane
@@ -561,14 +574,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         float m_ref = -INFINITY;  // reference maximum, base-2 scaled units
         float l = 0.0f;           // running sum of the weights p (fp32): gives lse
-        float lq = 0.0f;          // running sum of the weights as rounded for the
-                                  // product P V: O is divided by this one, so O is
-                                  // a convex combination of V rows with exactly the
-                                  // weights the tensor cores used
+        float lq = 0.0f;          // running sum used to normalise O: l with each
+                                  // tile's largest weight as rounded for P V
         bool ok = true;
 
+        // The two softmax warpgroups take turns (0, 1, 0, 1, ...): one runs its
+        // exponentials while the other tile's products occupy the tensor core.
+        if (w == 1 && lane == 0) mbar_arrive(bar(C::kBarTurn + 0));
         for (int j = 0; j < T; ++j) {
-            bool got = wait_phase(bar(C::kBarSFull + w), j & 1, abort_flag, p.err, 10);
+            bool got = wait_phase(bar(C::kBarSFull + w), j & 1, abort_flag, p, 10);
+            ok = __all_sync(0xffffffffu, got);
+            if (!ok) break;
+            got = wait_phase(bar(C::kBarTurn + w), j & 1, abort_flag, p, 13);
             ok = __all_sync(0xffffffffu, got);
             if (!ok) break;
             tc_fence_after();
@@ -605,18 +622,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float shift = (m_ref == -INFINITY) ? 0.0f : m_ref;
 
-            // p = 2^(s*c - shift) for the 128 keys, two at a time (f32x2);
-            // P goes to TMEM over the scores, the sums stay in registers
-            if (valid < kTileN) {
-                exp_tile<TF32, true>(s, c, shift, valid, tS, l, lq);
-            } else {
-                exp_tile<TF32, false>(s, c, shift, valid, tS, l, lq);
-            }
-
             if (j > 0 && __any_sync(0xffffffffu, need)) {
                 // O holds the previous tiles' contributions (their products
                 // completed before this tile's scores were signalled); the
-                // next product into O waits for this warp's arrival below.
+                // next product into O waits for this warp's first arrival.
 #pragma unroll
                 for (int q = 0; q < D / 32; ++q) {
                     uint32_t o[32];
@@ -633,15 +642,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32(tO + 32u * q, o);
                 }
             }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::kBarPFull + w));
+
+            // p = 2^(s*c - shift), two keys at a time (f32x2), written over
+            // the scores in two halves; each half is published on its own
+            // barrier so its products can start early
+            const uint64_t c2 = f2_pack(c, c);
+            const uint64_t ns2 = f2_pack(-shift, -shift);
+            uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (valid < kTileN) {
+                    exp_half<TF32, true>(s, c2, ns2, valid, tS, h, acc);
+                } else {
+                    exp_half<TF32, false>(s, c2, ns2, valid, tS, h, acc);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::kBarPFull + 2 * w + h));
+            }
+            if (lane == 0) mbar_arrive(bar(C::kBarTurn + (1 - w)));
+            // l: fp32 sum of the weights (gives lse).  lq: the same sum with
+            // the tile's largest weight replaced by its value as rounded for
+            // the P V product (bf16 or TF32; same FMA, exponential and
+            // rounding as the element itself).  A weight that dominates a
+            // row then enters the normalisation exactly as it entered O.
+            const float tsum = sum8(acc);
+            const float pmax = ex2(fmaf(mx, c, -shift));
+            const float pmax_r = TF32 ? u2f(round_tf32(pmax)) : u2f(pack_bf16x2(pmax, 0.0f) << 16);
+            l += tsum;
+            lq += tsum + (pmax_r - pmax);
         }
 
         // ------------------------------------------------------- epilogue
         if (ok) {
-            bool got = wait_phase(bar(C::kBarOFull + w), 0, abort_flag, p.err, 11);
+            bool got = wait_phase(bar(C::kBarOFull + w), 0, abort_flag, p, 11);
             ok = __all_sync(0xffffffffu, got);
         }
         const int row = row0 + w * kTileM + t;
@@ -690,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Every thread of the warpgroup arrives exactly once, whatever happened.
         mbar_arrive(bar(C::kBarEpi + w));
         if (t == 0) {
-            const bool all_in = wait_phase(bar(C::kBarEpi + w), 0, abort_flag, p.err, 12);
+            const bool all_in = wait_phase(bar(C::kBarEpi + w), 0, abort_flag, p, 12);
             // a tile lying entirely past N has nothing to store
             if (all_in && !*abort_flag && row0 + w * kTileM < p.N) {
                 for (int a = 0; a < C::kAtoms; ++a)

@@ -82,8 +82,21 @@ int fa_fwd_validate(const void* q, const void* k, const void* v, void* o,
  * fa_device_status — synchronise `stream`, then read and clear the device
  * error word the kernels set when a bounded wait gives up.  Returns FA_OK,
  * FA_ERR_TIMEOUT, or FA_ERR_CUDA if the synchronisation itself failed.
+ * A launch that timed out leaves its outputs incomplete (the CTAs of that
+ * launch stop early); later launches run normally whether or not the word
+ * has been read.
  */
 int fa_device_status(void* stream);
+
+/*
+ * fa_selftest_barrier_timeout — enqueue on `stream` a one-CTA kernel that
+ * waits, with the forward kernel's bounded barrier wait (about 1 s), on a
+ * barrier phase that nothing completes.  The wait gives up, the kernel exits
+ * normally and fa_device_status(stream) then returns FA_ERR_TIMEOUT (once).
+ * It exercises the failure-reporting path without faulting or hanging the
+ * GPU; the context stays usable.  Returns FA_OK or FA_ERR_CUDA (launch).
+ */
+int fa_selftest_barrier_timeout(void* stream);
 
 /* Static English text for a status code; never NULL. */
 const char* fa_status_string(int status);
