@@ -10,6 +10,7 @@ was not built.
 """
 from .binding import (FA_DTYPE_BF16, FA_DTYPE_F32, FA_ERR_ALIGNMENT, FA_ERR_CUDA,  # noqa: F401
                       FA_ERR_INVALID_ARG, FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED, FA_OK, FAError,
-                      attention, fa_device_status, fa_fwd, fa_fwd_validate,
+                      attention, fa_device_status, fa_fwd, fa_fwd_ex, fa_fwd_ex_splits,
+                      fa_fwd_ex_validate, fa_fwd_ex_workspace_size, fa_fwd_validate,
                       fa_last_error_message, fa_selftest_barrier_timeout, fa_status_string,
                       fa_version)

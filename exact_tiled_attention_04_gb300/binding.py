@@ -75,6 +75,17 @@ def load(path: str | None = None):
         lib.fa_version.argtypes = []
         lib.fa_selftest_barrier_timeout.restype = c_int
         lib.fa_selftest_barrier_timeout.argtypes = [vp]
+        sz = ctypes.c_size_t
+        lib.fa_fwd_ex.restype = c_int
+        lib.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, c_int, c_int,
+                                  vp, sz, vp]
+        lib.fa_fwd_ex_validate.restype = c_int
+        lib.fa_fwd_ex_validate.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, c_int,
+                                           c_int, vp, sz]
+        lib.fa_fwd_ex_workspace_size.restype = sz
+        lib.fa_fwd_ex_workspace_size.argtypes = [i64, i64, i64, i64, i64, c_int]
+        lib.fa_fwd_ex_splits.restype = c_int
+        lib.fa_fwd_ex_splits.argtypes = [i64, i64, i64, i64, c_int]
         _lib = lib
         return lib
 
@@ -96,6 +107,28 @@ def fa_fwd(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, N: i
 def fa_fwd_validate(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, N: int,
                     d: int, scale: float, dtype: int) -> int:
     return load().fa_fwd_validate(q, k, v, o, lse or None, B, H, N, d, scale, dtype)
+
+
+def fa_fwd_ex(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, H_kv: int,
+              N_q: int, N_kv: int, d: int, scale: float, dtype: int, num_splits: int,
+              workspace: int | None, workspace_bytes: int, stream: int | None) -> int:
+    return load().fa_fwd_ex(q, k, v, o, lse or None, B, H, H_kv, N_q, N_kv, d, scale, dtype,
+                            num_splits, workspace or None, workspace_bytes, stream or None)
+
+
+def fa_fwd_ex_validate(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int,
+                       H_kv: int, N_q: int, N_kv: int, d: int, scale: float, dtype: int,
+                       num_splits: int, workspace: int | None, workspace_bytes: int) -> int:
+    return load().fa_fwd_ex_validate(q, k, v, o, lse or None, B, H, H_kv, N_q, N_kv, d, scale,
+                                     dtype, num_splits, workspace or None, workspace_bytes)
+
+
+def fa_fwd_ex_workspace_size(B: int, H: int, N_q: int, N_kv: int, d: int, num_splits: int) -> int:
+    return int(load().fa_fwd_ex_workspace_size(B, H, N_q, N_kv, d, num_splits))
+
+
+def fa_fwd_ex_splits(B: int, H: int, N_q: int, N_kv: int, num_sms: int) -> int:
+    return int(load().fa_fwd_ex_splits(B, H, N_q, N_kv, num_sms))
 
 
 def fa_device_status(stream: int | None) -> int:

@@ -140,62 +140,123 @@ const char* fa_status_string(int status) {
 
 const char* fa_last_error_message(void) { return g_last_error; }
 
-int fa_fwd_validate(const void* q, const void* k, const void* v, void* o, const float* lse,
-                    int64_t B, int64_t H, int64_t N, int64_t d, float scale, int dtype) {
+}  // extern "C"
+
+namespace {
+
+// Effective key partitions for a requested count: at most one per key tile,
+// at most kMaxSplits, and no empty partition.
+struct SplitPlan {
+    int splits;
+    int tiles_per_split;
+    int n_kv_tiles;
+};
+constexpr int kMaxSplits = 32;  // the merge kernel holds one partition per lane
+
+SplitPlan plan_splits(int64_t N_kv, int num_splits) {
+    SplitPlan sp;
+    sp.n_kv_tiles = static_cast<int>((N_kv + 127) / 128);
+    int s = num_splits < 1 ? 1 : num_splits;
+    if (s > kMaxSplits) s = kMaxSplits;
+    if (s > sp.n_kv_tiles) s = sp.n_kv_tiles;
+    sp.tiles_per_split = (sp.n_kv_tiles + s - 1) / s;
+    sp.splits = (sp.n_kv_tiles + sp.tiles_per_split - 1) / sp.tiles_per_split;
+    return sp;
+}
+
+size_t workspace_bytes_for(int64_t B, int64_t H, int64_t N_q, int64_t d, const SplitPlan& sp) {
+    if (sp.splits <= 1) return 0;
+    const size_t rows = static_cast<size_t>(B) * static_cast<size_t>(H) * static_cast<size_t>(N_q);
+    return static_cast<size_t>(sp.splits) * rows * (static_cast<size_t>(d) + 4) * sizeof(float);
+}
+
+int validate_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d,
+                float scale, int dtype, int num_splits, const void* workspace,
+                size_t workspace_bytes) {
     if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
-    if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || H_kv < 1 || N_q < 1 || N_kv < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (H % H_kv != 0) return FA_ERR_INVALID_ARG;
+    if (num_splits < 1) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
     if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
     if (dtype == FA_DTYPE_BF16 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     if (dtype == FA_DTYPE_F32 && d != 64) return FA_ERR_UNSUPPORTED;
-    // element count and byte size must fit in int64 (d is 64 or 128 here)
+    // element counts and byte sizes must fit in int64 (d is 64 or 128 here)
     if (B > INT64_MAX / H) return FA_ERR_INVALID_ARG;
-    const int64_t BH = B * H;
-    if (BH > INT64_MAX / N || BH * N > INT64_MAX / (d * 4)) return FA_ERR_INVALID_ARG;
+    const int64_t BH = B * H, BHkv = B * H_kv;
+    if (BH > INT64_MAX / N_q || BH * N_q > INT64_MAX / (d * 4)) return FA_ERR_INVALID_ARG;
+    if (BHkv > INT64_MAX / N_kv || BHkv * N_kv > INT64_MAX / (d * 4)) return FA_ERR_INVALID_ARG;
     // TMA coordinates are 32-bit; global strides below 2^40 bytes
-    if (BH > kInt32Max || N > kInt32Max) return FA_ERR_UNSUPPORTED;
+    if (BH > kInt32Max || N_q > kInt32Max || N_kv > kInt32Max) return FA_ERR_UNSUPPORTED;
     const int64_t elem = dtype == FA_DTYPE_BF16 ? 2 : 4;
-    if (N * d * elem >= (int64_t(1) << 40)) return FA_ERR_UNSUPPORTED;
-    const int64_t qblocks = (N + 255) / 256;
-    if (qblocks > kInt32Max / BH) return FA_ERR_UNSUPPORTED;  // one CTA per 256 rows
+    if (N_q * d * elem >= (int64_t(1) << 40) || N_kv * d * elem >= (int64_t(1) << 40))
+        return FA_ERR_UNSUPPORTED;
+    const SplitPlan sp = plan_splits(N_kv, num_splits);
+    const int64_t qblocks = (N_q + 255) / 256;
+    if (qblocks * sp.splits > kInt32Max / BH) return FA_ERR_UNSUPPORTED;  // one CTA per 256 rows per partition
     const uintptr_t mask = 15;
     if ((reinterpret_cast<uintptr_t>(q) & mask) || (reinterpret_cast<uintptr_t>(k) & mask) ||
         (reinterpret_cast<uintptr_t>(v) & mask) || (reinterpret_cast<uintptr_t>(o) & mask))
         return FA_ERR_ALIGNMENT;
     if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3)) return FA_ERR_ALIGNMENT;
-    const size_t bytes = static_cast<size_t>(BH * N * d * elem);
-    if (overlaps(o, bytes, q, bytes) || overlaps(o, bytes, k, bytes) || overlaps(o, bytes, v, bytes))
+    const size_t qbytes = static_cast<size_t>(BH * N_q * d * elem);
+    const size_t kvbytes = static_cast<size_t>(BHkv * N_kv * d * elem);
+    if (overlaps(o, qbytes, q, qbytes) || overlaps(o, qbytes, k, kvbytes) || overlaps(o, qbytes, v, kvbytes))
         return FA_ERR_INVALID_ARG;
     if (lse != nullptr) {
-        const size_t lbytes = static_cast<size_t>(BH * N) * sizeof(float);
-        if (overlaps(lse, lbytes, o, bytes) || overlaps(lse, lbytes, q, bytes) ||
-            overlaps(lse, lbytes, k, bytes) || overlaps(lse, lbytes, v, bytes))
+        const size_t lbytes = static_cast<size_t>(BH * N_q) * sizeof(float);
+        if (overlaps(lse, lbytes, o, qbytes) || overlaps(lse, lbytes, q, qbytes) ||
+            overlaps(lse, lbytes, k, kvbytes) || overlaps(lse, lbytes, v, kvbytes))
+            return FA_ERR_INVALID_ARG;
+    }
+    const size_t need = workspace_bytes_for(B, H, N_q, d, sp);
+    if (need > 0) {
+        if (workspace == nullptr || workspace_bytes < need) return FA_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(workspace) & mask) return FA_ERR_ALIGNMENT;
+        if (overlaps(workspace, need, o, qbytes) || overlaps(workspace, need, q, qbytes) ||
+            overlaps(workspace, need, k, kvbytes) || overlaps(workspace, need, v, kvbytes) ||
+            (lse != nullptr && overlaps(workspace, need, lse, static_cast<size_t>(BH * N_q) * sizeof(float))))
             return FA_ERR_INVALID_ARG;
     }
     return FA_OK;
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
-           int64_t N, int64_t d, float scale, int dtype, void* stream) {
-    int st = fa_fwd_validate(q, k, v, o, lse, B, H, N, d, scale, dtype);
-    if (st != FA_OK) return st;
+int launch_ex(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+              int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d, float scale, int dtype,
+              int num_splits, void* workspace, void* stream) {
     const int64_t BH = B * H;
+    const SplitPlan sp = plan_splits(N_kv, num_splits);
     CUtensorMap mq, mk, mv, mo;
-    if ((st = encode_map(&mq, q, dtype, BH, N, d)) != FA_OK) return st;
-    if ((st = encode_map(&mk, k, dtype, BH, N, d)) != FA_OK) return st;
-    if ((st = encode_map(&mv, v, dtype, BH, N, d)) != FA_OK) return st;
-    if ((st = encode_map(&mo, o, dtype, BH, N, d)) != FA_OK) return st;
+    int st;
+    if ((st = encode_map(&mq, q, dtype, BH, N_q, d)) != FA_OK) return st;
+    if ((st = encode_map(&mk, k, dtype, B * H_kv, N_kv, d)) != FA_OK) return st;
+    if ((st = encode_map(&mv, v, dtype, B * H_kv, N_kv, d)) != FA_OK) return st;
+    if ((st = encode_map(&mo, o, dtype, BH, N_q, d)) != FA_OK) return st;
 
-    fa::FwdParams p;
-    p.lse = lse;
+    fa::FwdParams p{};
     p.status = device_status_words(&st);
     if (st != FA_OK) return st;
     p.gen = next_generation();
-    p.N = static_cast<int>(N);
-    p.n_kv_tiles = static_cast<int>((N + 127) / 128);
-    p.n_q_blocks = static_cast<int>((N + 255) / 256);
+    p.Nq = static_cast<int>(N_q);
+    p.Nkv = static_cast<int>(N_kv);
+    p.n_kv_tiles = sp.n_kv_tiles;
+    p.n_q_blocks = static_cast<int>((N_q + 255) / 256);
+    p.H = static_cast<int>(H);
+    p.H_kv = static_cast<int>(H_kv);
+    p.group = static_cast<int>(H / H_kv);
+    p.splits = sp.splits;
+    p.tiles_per_split = sp.tiles_per_split;
     p.scale_log2 = scale * 1.4426950408889634f;
-    const unsigned int grid = static_cast<unsigned int>(BH * p.n_q_blocks);
+    const size_t rows = static_cast<size_t>(BH) * static_cast<size_t>(N_q);
+    if (sp.splits > 1) {
+        p.o_part = static_cast<float*>(workspace);
+        p.ml_part = p.o_part + static_cast<size_t>(sp.splits) * rows * static_cast<size_t>(d);
+        p.lse = nullptr;
+    } else {
+        p.lse = lse;
+    }
+    const unsigned int grid = static_cast<unsigned int>(BH * p.n_q_blocks * sp.splits);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     cudaError_t e;
@@ -205,11 +266,69 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
         e = fa::launch_fwd_bf16_d128(mq, mk, mv, mo, p, grid, s);
     else
         e = fa::launch_fwd_tf32_d64(mq, mk, mv, mo, p, grid, s);
+    if (e == cudaSuccess && sp.splits > 1) {
+        fa::MergeParams m{};
+        m.o_part = p.o_part;
+        m.ml_part = p.ml_part;
+        m.o = o;
+        m.lse = lse;
+        m.rows = static_cast<long long>(rows);
+        m.splits = sp.splits;
+        e = fa::launch_merge(m, static_cast<int>(d), dtype, s);
+    }
     if (e != cudaSuccess) {
         set_error("fa_fwd launch", static_cast<int>(e), cudaGetErrorString(e));
         return FA_ERR_CUDA;
     }
     return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd_validate(const void* q, const void* k, const void* v, void* o, const float* lse,
+                    int64_t B, int64_t H, int64_t N, int64_t d, float scale, int dtype) {
+    return validate_ex(q, k, v, o, lse, B, H, H, N, N, d, scale, dtype, 1, nullptr, 0);
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+           int64_t N, int64_t d, float scale, int dtype, void* stream) {
+    const int st = validate_ex(q, k, v, o, lse, B, H, H, N, N, d, scale, dtype, 1, nullptr, 0);
+    if (st != FA_OK) return st;
+    return launch_ex(q, k, v, o, lse, B, H, H, N, N, d, scale, dtype, 1, nullptr, stream);
+}
+
+int fa_fwd_ex_validate(const void* q, const void* k, const void* v, void* o, const float* lse,
+                       int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d,
+                       float scale, int dtype, int num_splits, const void* workspace,
+                       size_t workspace_bytes) {
+    return validate_ex(q, k, v, o, lse, B, H, H_kv, N_q, N_kv, d, scale, dtype, num_splits,
+                       workspace, workspace_bytes);
+}
+
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+              int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d, float scale, int dtype,
+              int num_splits, void* workspace, size_t workspace_bytes, void* stream) {
+    const int st = validate_ex(q, k, v, o, lse, B, H, H_kv, N_q, N_kv, d, scale, dtype, num_splits,
+                               workspace, workspace_bytes);
+    if (st != FA_OK) return st;
+    return launch_ex(q, k, v, o, lse, B, H, H_kv, N_q, N_kv, d, scale, dtype, num_splits, workspace,
+                     stream);
+}
+
+size_t fa_fwd_ex_workspace_size(int64_t B, int64_t H, int64_t N_q, int64_t N_kv, int64_t d,
+                                int num_splits) {
+    if (B < 1 || H < 1 || N_q < 1 || N_kv < 1 || d < 1) return 0;
+    return workspace_bytes_for(B, H, N_q, d, plan_splits(N_kv, num_splits));
+}
+
+int fa_fwd_ex_splits(int64_t B, int64_t H, int64_t N_q, int64_t N_kv, int num_sms) {
+    if (B < 1 || H < 1 || N_q < 1 || N_kv < 1 || num_sms < 1) return 1;
+    const int64_t ctas = B * H * ((N_q + 255) / 256);
+    if (ctas >= num_sms) return 1;
+    const int64_t want = num_sms / ctas;  // fill about one wave
+    return plan_splits(N_kv, static_cast<int>(want > kMaxSplits ? kMaxSplits : want)).splits;
 }
 
 int fa_device_status(void* stream) {

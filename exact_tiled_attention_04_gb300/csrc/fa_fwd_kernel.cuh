@@ -101,6 +101,14 @@ struct FwdCfg {
     static constexpr int kPvSplit = 1;
     static constexpr uint32_t kIdescPV = instr_desc(kFmt, false, !TF32, kTileM, kPvN);
 
+    // The other softmax warpgroup may start once this one has published
+    // half kTurnAfterHalf of P.  d = 128: after the whole tile (strict
+    // alternation keeps the tensor core fed); d = 64: after the first half
+    // (the products are short, the exponentials dominate, so overlapping the
+    // two warpgroups' exponentials wins; measured +7 % at d = 64, -7 % at
+    // d = 128).
+    static constexpr int kTurnAfterHalf = (D == 64) ? 0 : 1;
+
     // register split (setmaxnreg): softmax warpgroups / warpgroup 2, chosen
     // so that neither side spills
     static constexpr uint32_t kSoftmaxRegs = TF32 ? 200 : 208;
@@ -248,6 +256,34 @@ __device__ __forceinline__ float sum8(const uint64_t (&a)[4]) {
     return ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
 }
 
+// Epilogue of one key partition of a split launch (one thread = one query
+// row): the unnormalised accumulator, relative to the reference maximum m,
+// and m, l, lq go to the partition's slab of the workspace.  Not inlined: it
+// runs once per CTA and keeps its address arithmetic out of the main loop.
+template <int D>
+__device__ __noinline__ void store_partial(const FwdParams& p, uint32_t tO, int row, float m_ref,
+                                           float l, float lq) {
+    const unsigned int split = blockIdx.x % static_cast<unsigned>(p.splits);
+    const unsigned int cta = blockIdx.x / static_cast<unsigned>(p.splits);
+    const size_t bh = cta / static_cast<unsigned>(p.n_q_blocks);
+    // rows of one partition's slab: B*H*Nq (the grid holds B*H*n_q_blocks*splits CTAs)
+    const size_t slab = static_cast<size_t>(gridDim.x / p.splits / p.n_q_blocks) * p.Nq;
+    const size_t r = split * slab + bh * p.Nq + row;
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32u * q, o);
+        tmem_ld_wait(o);
+        if (row < p.Nq) {
+            uint4* dst = reinterpret_cast<uint4*>(p.o_part + r * D + q * 32);
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                dst[ch] = make_uint4(o[4 * ch], o[4 * ch + 1], o[4 * ch + 2], o[4 * ch + 3]);
+        }
+    }
+    if (row < p.Nq) *reinterpret_cast<float4*>(p.ml_part + r * 4) = make_float4(m_ref, l, lq, 0.0f);
+}
+
 // Round `n16` 16-byte groups of fp32 in shared memory to TF32 in place
 // (round to nearest, ties away), one warp.
 __device__ __forceinline__ void round_tf32_inplace(uint8_t* base, int n16, int lane) {
@@ -294,7 +330,7 @@ __device__ __forceinline__ void transpose_v_tf32(const uint8_t* vraw, uint8_t* v
 template <int D>
 __device__ void produce_tf32(const CUtensorMap& map_q, const CUtensorMap& map_k,
                              const CUtensorMap& map_v, const FwdParams& p, uint8_t* smem,
-                             uint32_t sbase, int lane, int row0, int bh, int T,
+                             uint32_t sbase, int lane, int row0, int bh, int kvh, int t_begin, int T,
                              volatile uint32_t* abort_flag) {
     using C = FwdCfg<true, D>;
     auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * static_cast<uint32_t>(i); };
@@ -328,12 +364,12 @@ __device__ void produce_tf32(const CUtensorMap& map_q, const CUtensorMap& map_k,
             mbar_arrive_expect_tx(bar(C::kBarKRaw + ks), C::kTileBytes);
             for (int a = 0; a < C::kAtoms; ++a)
                 tma_load_3d(sbase + C::kOffK + ks * C::kTileBytes + a * C::kAtomBytes, &map_k,
-                            bar(C::kBarKRaw + ks), a * C::kAtomElems, j * kTileN, bh, keep);
+                            bar(C::kBarKRaw + ks), a * C::kAtomElems, (t_begin + j) * kTileN, kvh, keep);
             // the raw V buffer was fully read by this warp's previous transpose
             mbar_arrive_expect_tx(bar(C::kBarVRaw), C::kTileBytes);
             for (int a = 0; a < C::kAtoms; ++a)
                 tma_load_3d(sbase + C::kOffVRaw + a * C::kAtomBytes, &map_v, bar(C::kBarVRaw),
-                            a * C::kAtomElems, j * kTileN, bh, keep);
+                            a * C::kAtomElems, (t_begin + j) * kTileN, kvh, keep);
         }
         nk = j + 1;
         nv = j + 1;
@@ -377,10 +413,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = static_cast<int>(threadIdx.x) / 32;
     const int lane = static_cast<int>(threadIdx.x) % 32;
-    const int qb = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.n_q_blocks));
-    const int bh = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.n_q_blocks));
+    // blockIdx.x = ((bh * n_q_blocks) + qb) * splits + split
+    const unsigned int split = blockIdx.x % static_cast<unsigned>(p.splits);
+    const unsigned int cta = blockIdx.x / static_cast<unsigned>(p.splits);
+    const int qb = static_cast<int>(cta % static_cast<unsigned>(p.n_q_blocks));
+    const int bh = static_cast<int>(cta / static_cast<unsigned>(p.n_q_blocks));
+    // key/value head of this query head (grouped-query attention: H / H_kv
+    // query heads share one key/value head)
+    const int kvh = (bh / p.H) * p.H_kv + (bh % p.H) / p.group;
     const int row0 = qb * 2 * kTileM;
-    const int T = p.n_kv_tiles;
+    const int t_begin = static_cast<int>(split) * p.tiles_per_split;
+    const int T = min(p.tiles_per_split, p.n_kv_tiles - t_begin);  // >= 1 (host guarantees)
 
     auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * static_cast<uint32_t>(i); };
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kOffAbort);
@@ -437,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp == kLoadWarp) {
         // ------------------------------------------------------ TMA producer
         if constexpr (TF32) {
-            produce_tf32<D>(map_q, map_k, map_v, p, smem, sbase, lane, row0, bh, T, abort_flag);
+            produce_tf32<D>(map_q, map_k, map_v, p, smem, sbase, lane, row0, bh, kvh, t_begin, T, abort_flag);
         } else if (lane == 0) {
             const uint64_t keep = policy_evict_last();   // K/V: read by every query block of the head
             const uint64_t once = policy_evict_first();  // Q: read once
@@ -454,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(bar(C::kBarKFull + ks), C::kTileBytes);
                 for (int a = 0; a < C::kAtoms; ++a)
                     tma_load_3d(sbase + C::kOffK + ks * C::kTileBytes + a * C::kAtomBytes, &map_k,
-                                bar(C::kBarKFull + ks), a * C::kAtomElems, j * kTileN, bh, keep);
+                                bar(C::kBarKFull + ks), a * C::kAtomElems, (t_begin + j) * kTileN, kvh, keep);
                 nk = j + 1;
                 const int vs = j % C::kVStages;
                 if (!wait_phase(bar(C::kBarVEmpty + vs), ((j / C::kVStages) & 1) ^ 1, abort_flag, p, 2))
@@ -462,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(bar(C::kBarVFull + vs), C::kTileBytes);
                 for (int a = 0; a < C::kAtoms; ++a)
                     tma_load_3d(sbase + C::kOffV + vs * C::kTileBytes + a * C::kAtomBytes, &map_v,
-                                bar(C::kBarVFull + vs), a * C::kAtomElems, j * kTileN, bh, keep);
+                                bar(C::kBarVFull + vs), a * C::kAtomElems, (t_begin + j) * kTileN, kvh, keep);
                 nv = j + 1;
             }
             // Drain: wait until every issued load has landed, so that no TMA
@@ -579,7 +622,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
 
         // The two softmax warpgroups take turns (0, 1, 0, 1, ...): one runs its
-        // exponentials while the other tile's products occupy the tensor core.
+        // exponentials while the other tile's products occupy the tensor core
+        // (see kTurnAfterHalf for how far the turns overlap).
         if (w == 1 && lane == 0) mbar_arrive(bar(C::kBarTurn + 0));
         for (int j = 0; j < T; ++j) {
             bool got = wait_phase(bar(C::kBarSFull + w), j & 1, abort_flag, p, 10);
@@ -596,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q) tmem_ld_wait(s[q]);
 
-            const int valid = p.N - j * kTileN;  // keys of this tile inside the sequence
+            const int valid = p.Nkv - (t_begin + j) * kTileN;  // keys of this tile inside the sequence
             if (valid < kTileN) {
                 // keys past N: copy key 0's score so they cannot win the max;
                 // their weight is zeroed below
@@ -660,8 +704,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::kBarPFull + 2 * w + h));
+                if (h == C::kTurnAfterHalf && lane == 0) mbar_arrive(bar(C::kBarTurn + (1 - w)));
             }
-            if (lane == 0) mbar_arrive(bar(C::kBarTurn + (1 - w)));
             // l: fp32 sum of the weights (gives lse).  lq: the same sum with
             // the tile's largest weight replaced by its value as rounded for
             // the P V product (bf16 or TF32; same FMA, exponential and
@@ -681,7 +725,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int row = row0 + w * kTileM + t;
         uint8_t* stage = smem + C::kOffQ + w * C::kTileBytes;  // Q_w is free after its last S MMA
-        if (ok) {
+        const bool split_mode = p.splits > 1;
+        if (ok && split_mode) {
+            tc_fence_after();
+            store_partial<D>(p, tO, row, m_ref, l, lq);
+        }
+        if (ok && !split_mode) {
             tc_fence_after();
             const float inv_l = lq > 0.0f ? 1.0f / lq : 0.0f;
 #pragma unroll
@@ -716,9 +765,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (p.lse != nullptr && row < p.N) {
+            if (p.lse != nullptr && row < p.Nq) {
                 const float lse2 = (l > 0.0f) ? (m_ref + log2f(l)) : -INFINITY;
-                p.lse[static_cast<size_t>(bh) * static_cast<size_t>(p.N) + row] = lse2 * 0.69314718055994531f;
+                p.lse[static_cast<size_t>(bh) * static_cast<size_t>(p.Nq) + row] = lse2 * 0.69314718055994531f;
             }
             fence_proxy_async_smem();
         }
@@ -726,8 +775,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(C::kBarEpi + w));
         if (t == 0) {
             const bool all_in = wait_phase(bar(C::kBarEpi + w), 0, abort_flag, p, 12);
-            // a tile lying entirely past N has nothing to store
-            if (all_in && !*abort_flag && row0 + w * kTileM < p.N) {
+            // a tile lying entirely past Nq has nothing to store
+            if (all_in && !split_mode && !*abort_flag && row0 + w * kTileM < p.Nq) {
                 for (int a = 0; a < C::kAtoms; ++a)
                     tma_store_3d(&map_o, smem_u32(stage + a * C::kAtomBytes), a * C::kAtomElems,
                                  row0 + w * kTileM, bh);

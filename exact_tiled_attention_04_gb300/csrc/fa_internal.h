@@ -16,13 +16,33 @@ struct DevStatus {
 
 // Parameters of one forward launch, passed by value.
 struct FwdParams {
-    float* lse;              // fp32 [BH, N] or nullptr
+    float* lse;              // fp32 [B*H, Nq] or nullptr (unsplit launches)
     DevStatus* status;       // device status word of the current device
     unsigned int gen;        // this launch's generation (never 0)
-    int N;                   // sequence length
-    int n_kv_tiles;          // ceil(N / 128)
-    int n_q_blocks;          // ceil(N / 256): query blocks per (b, h)
+    int Nq;                  // query rows per head
+    int Nkv;                 // key / value rows per head
+    int n_kv_tiles;          // ceil(Nkv / 128)
+    int n_q_blocks;          // ceil(Nq / 256): query blocks per (b, h)
+    int H;                   // query heads
+    int group;               // query heads per key/value head (H / H_kv)
+    int H_kv;                // key / value heads
+    int splits;              // key-range partitions per query block (1 = none)
+    int tiles_per_split;     // key tiles per partition
     float scale_log2;        // scale * log2(e)
+    // splits > 1: unnormalised partial results, one slab per partition
+    float* o_part;           // fp32 [splits, B*H, Nq, d]
+    float* ml_part;          // fp32 [splits, B*H, Nq, 4]: m (base 2, scaled), l, lq, unused
+};
+
+// Merge of split partial results: O = sum_s w_s O_s / sum_s w_s lq_s,
+// lse = ln 2 * (M + log2 sum_s w_s l_s), w_s = 2^(m_s - M), M = max_s m_s.
+struct MergeParams {
+    const float* o_part;
+    const float* ml_part;
+    void* o;                 // [B*H, Nq, d] in the output dtype
+    float* lse;              // [B*H, Nq] or nullptr
+    long long rows;          // B*H*Nq
+    int splits;
 };
 
 // Device error word bits.
@@ -37,7 +57,10 @@ size_t fwd_smem_bytes_bf16_d64();
 size_t fwd_smem_bytes_bf16_d128();
 size_t fwd_smem_bytes_tf32_d64();
 
-// Launchers: one CTA per 256 query rows of one (b, h); 384 threads.
+cudaError_t launch_merge(const MergeParams& m, int d, int dtype, cudaStream_t stream);
+
+// Launchers: one CTA per 256 query rows of one (b, h) and key partition;
+// 384 threads.
 cudaError_t launch_fwd_bf16_d64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                 const CUtensorMap& o, const FwdParams& p, unsigned int grid,
                                 cudaStream_t stream);

@@ -230,3 +230,15 @@ def sample_rows(w: Workload, count: int, seed_offset: int = 0) -> np.ndarray:
     rows[:, 1] = (u[:, 1] % np.uint64(w.H)).astype(np.int64)
     rows[:, 2] = (u[:, 2] % np.uint64(w.N)).astype(np.int64)
     return rows
+
+
+def make_general(B: int, H: int, H_kv: int, Nq: int, Nkv: int, d: int, dtype: str = "bf16",
+                 seed: int = 13, factor: float = 1.0):
+    """Seeded q [B, H, Nq, d] and k, v [B, H_kv, Nkv, d] (grouped key/value
+    heads, separate query and key lengths), rounded like make()."""
+    out = []
+    for t, shape in ((TENSOR_Q, (B, H, Nq, d)), (TENSOR_K, (B, H_kv, Nkv, d)),
+                     (TENSOR_V, (B, H_kv, Nkv, d))):
+        n = shape[0] * shape[1] * shape[2] * shape[3]
+        out.append(_finish(normals(seed, t, n, factor).reshape(shape), dtype))
+    return tuple(out)

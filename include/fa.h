@@ -19,6 +19,7 @@
 #ifndef FA_GB300_H
 #define FA_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -77,6 +78,59 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 int fa_fwd_validate(const void* q, const void* k, const void* v, void* o,
                     const float* lse, int64_t B, int64_t H, int64_t N,
                     int64_t d, float scale, int dtype);
+
+/*
+ * fa_fwd_ex — the general form: decode shapes, grouped-query heads and
+ * key-range partitions ("split-KV").
+ *
+ *   q, o    : [B, H, N_q, d] of `dtype`;   k, v : [B, H_kv, N_kv, d];
+ *   lse     : fp32 [B, H, N_q] or NULL.
+ *   H_kv    : key/value heads, dividing H; query head h reads key/value
+ *             head h / (H / H_kv) (grouped-query attention; H_kv = H is
+ *             ordinary multi-head attention).
+ *   N_q, N_kv: query rows and key/value rows per head (N_q = 1 is a decode
+ *             step against a cache of N_kv keys, the FlashDecoding case of
+ *             "FlashAttention dissected", section "Interaction with the KV
+ *             cache during inference").
+ *   num_splits: >= 1 key-range partitions per query block.  1 runs the fused
+ *             kernel alone.  More partitions sweep disjoint key ranges in
+ *             separate CTAs, which then fill the GPU when B * H * N_q is
+ *             small; their partial results go to `workspace` and a second
+ *             kernel merges them with the online-softmax rescaling.  The
+ *             count is capped at 32 and at one partition per 128 keys.
+ *   workspace, workspace_bytes: device scratch owned by the caller, 16-byte
+ *             aligned, at least fa_fwd_ex_workspace_size(...) bytes; may be
+ *             NULL when that size is 0.  Contents on entry do not matter.
+ *
+ * Same ownership, validation and error behaviour as fa_fwd; the workspace
+ * must not overlap any tensor.  Both kernels are enqueued on `stream`.
+ */
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+              int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv,
+              int64_t d, float scale, int dtype, int num_splits,
+              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Host-side argument checks of fa_fwd_ex alone (no CUDA call). */
+int fa_fwd_ex_validate(const void* q, const void* k, const void* v, void* o,
+                       const float* lse, int64_t B, int64_t H, int64_t H_kv,
+                       int64_t N_q, int64_t N_kv, int64_t d, float scale,
+                       int dtype, int num_splits, const void* workspace,
+                       size_t workspace_bytes);
+
+/*
+ * Workspace bytes fa_fwd_ex needs for `num_splits` (after the same capping):
+ * splits * B * H * N_q * (d + 4) * 4, or 0 when one partition remains.
+ * Pure host computation; 0 for invalid sizes.
+ */
+size_t fa_fwd_ex_workspace_size(int64_t B, int64_t H, int64_t N_q, int64_t N_kv,
+                                int64_t d, int num_splits);
+
+/*
+ * A partition count that fills about one wave of `num_sms` SMs: 1 when
+ * B * H * ceil(N_q / 256) CTAs already fill the GPU, else
+ * num_sms / that count (capped as above).  Pure host computation.
+ */
+int fa_fwd_ex_splits(int64_t B, int64_t H, int64_t N_q, int64_t N_kv, int num_sms);
 
 /*
  * fa_device_status — synchronise `stream`, then read and clear the device

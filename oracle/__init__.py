@@ -61,6 +61,12 @@ def _bind(path: str):
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
     lib.oracle_default_threads.restype = ctypes.c_int
     lib.oracle_default_threads.argtypes = []
+    lib.oracle_attention_f64_ex.restype = ctypes.c_int
+    lib.oracle_attention_f64_ex.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int64,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
     return lib
 
 
@@ -113,6 +119,37 @@ def attention_f64(q, k, v, scale: float, rows=None, threads: int = 0, lib=None):
         raise ValueError(f"oracle_attention_f64 failed with status {rc}")
     if rows is None:
         return o.reshape(B, H, N, d), lse.reshape(B, H, N)
+    return o, lse
+
+
+def attention_f64_ex(q, k, v, scale: float, rows=None, threads: int = 0, lib=None):
+    """Exact attention in fp64, general shapes: q [B, H, Nq, d], k and v
+    [B, H_kv, Nkv, d] with H_kv dividing H (query head h uses key/value head
+    h // (H // H_kv)).  Returns (o, lse): [B, H, Nq, d] and [B, H, Nq] for
+    rows=None, else [R, d] and [R] for the (b, h, i) triples in `rows`."""
+    lib = lib or load()
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    k = np.ascontiguousarray(k, dtype=np.float32)
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    if q.ndim != 4 or k.ndim != 4 or k.shape != v.shape or q.shape[0] != k.shape[0] \
+            or q.shape[3] != k.shape[3]:
+        raise ValueError(f"incompatible shapes: q {q.shape}, k {k.shape}, v {v.shape}")
+    B, H, Nq, d = (int(x) for x in q.shape)
+    H_kv, Nkv = int(k.shape[1]), int(k.shape[2])
+    if rows is None:
+        nrows, rows_ptr = B * H * Nq, None
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1, 3)
+        nrows, rows_ptr = rows_arr.shape[0], rows_arr.ctypes.data
+    o = np.empty((nrows, d), dtype=np.float64)
+    lse = np.empty((nrows,), dtype=np.float64)
+    rc = lib.oracle_attention_f64_ex(q.ctypes.data, k.ctypes.data, v.ctypes.data, B, H, H_kv, Nq,
+                                     Nkv, d, float(scale), rows_ptr, nrows, o.ctypes.data,
+                                     lse.ctypes.data, int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_f64_ex failed with status {rc}")
+    if rows is None:
+        return o.reshape(B, H, Nq, d), lse.reshape(B, H, Nq)
     return o, lse
 
 

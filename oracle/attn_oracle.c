@@ -128,7 +128,7 @@ static void attention_row(const float *q_row, const float *k_head,
 
 typedef struct {
     const float *q, *k, *v;
-    int64_t B, H, N, d;
+    int64_t B, H, H_kv, Nq, N, d; /* N = key/value rows per head */
     double scale;
     const int64_t *rows; /* nrows * 3 entries (b, h, i), or NULL = all */
     int64_t nrows;
@@ -152,12 +152,15 @@ static void *worker(void *arg)
             h = jb->rows[3 * r + 1];
             i = jb->rows[3 * r + 2];
         } else {
-            i = r % jb->N;
-            h = (r / jb->N) % jb->H;
-            b = r / (jb->N * jb->H);
+            i = r % jb->Nq;
+            h = (r / jb->Nq) % jb->H;
+            b = r / (jb->Nq * jb->H);
         }
-        const int64_t head = (b * jb->H + h) * jb->N * jb->d;
-        attention_row(jb->q + head + i * jb->d, jb->k + head, jb->v + head,
+        /* query head h reads key/value head h / (H / H_kv) */
+        const int64_t kvh = b * jb->H_kv + h / (jb->H / jb->H_kv);
+        const float *q_row = jb->q + ((b * jb->H + h) * jb->Nq + i) * jb->d;
+        const int64_t kv_head = kvh * jb->N * jb->d;
+        attention_row(q_row, jb->k + kv_head, jb->v + kv_head,
                       jb->N, jb->d, jb->scale, s, jb->o + r * jb->d,
                       jb->lse + r);
     }
@@ -173,29 +176,36 @@ int oracle_default_threads(void)
 }
 
 /*
- * Exact attention in fp64 for the selected rows.
- *   q, k, v : fp32 [B, H, N, d]
+ * Exact attention in fp64 for the selected rows, general shapes:
+ *   q       : fp32 [B, H, Nq, d];   k, v : fp32 [B, H_kv, Nkv, d]
+ *   query head h attends with key/value head h / (H / H_kv) (H_kv divides
+ *   H; H_kv = H is plain multi-head attention).  Nq may differ from Nkv
+ *   (Nq = 1: one decode step against Nkv cached keys, as in the FlashDecoding
+ *   paragraph of "FlashAttention dissected", section "Interaction with the KV
+ *   cache during inference").
  *   rows    : NULL for every row (output order b, h, i), else nrows triples
  *             (b, h, i); out-of-range triples return -1.
  *   o       : fp64 [nrows, d];  lse : fp64 [nrows]
  *   threads : worker count, 0 = every online core.
  * Returns 0, or -1 on a bad argument, -2 when memory runs out.
  */
-int oracle_attention_f64(const float *q, const float *k, const float *v,
-                         int64_t B, int64_t H, int64_t N, int64_t d,
-                         double scale, const int64_t *rows, int64_t nrows,
-                         double *o, double *lse, int threads)
+int oracle_attention_f64_ex(const float *q, const float *k, const float *v,
+                            int64_t B, int64_t H, int64_t H_kv, int64_t Nq,
+                            int64_t Nkv, int64_t d, double scale,
+                            const int64_t *rows, int64_t nrows, double *o,
+                            double *lse, int threads)
 {
-    if (!q || !k || !v || !o || !lse || B < 1 || H < 1 || N < 1 || d < 1)
+    if (!q || !k || !v || !o || !lse || B < 1 || H < 1 || H_kv < 1 || H % H_kv != 0 ||
+        Nq < 1 || Nkv < 1 || d < 1)
         return -1;
     if (!rows)
-        nrows = B * H * N;
+        nrows = B * H * Nq;
     if (nrows < 0)
         return -1;
     if (rows) {
         for (int64_t r = 0; r < nrows; ++r) {
             const int64_t *t = rows + 3 * r;
-            if (t[0] < 0 || t[0] >= B || t[1] < 0 || t[1] >= H || t[2] < 0 || t[2] >= N)
+            if (t[0] < 0 || t[0] >= B || t[1] < 0 || t[1] >= H || t[2] < 0 || t[2] >= Nq)
                 return -1;
         }
     }
@@ -216,7 +226,7 @@ int oracle_attention_f64(const float *q, const float *k, const float *v,
     for (int t = 0; t < threads; ++t) {
         job_t *jb = &jobs[t];
         jb->q = q; jb->k = k; jb->v = v;
-        jb->B = B; jb->H = H; jb->N = N; jb->d = d;
+        jb->B = B; jb->H = H; jb->H_kv = H_kv; jb->Nq = Nq; jb->N = Nkv; jb->d = d;
         jb->scale = scale;
         jb->rows = rows;
         jb->nrows = nrows;
@@ -245,4 +255,14 @@ int oracle_attention_f64(const float *q, const float *k, const float *v,
     free(jobs);
     free(tids);
     return status;
+}
+
+/* Square self-attention form: q, k, v all [B, H, N, d]. */
+int oracle_attention_f64(const float *q, const float *k, const float *v,
+                         int64_t B, int64_t H, int64_t N, int64_t d,
+                         double scale, const int64_t *rows, int64_t nrows,
+                         double *o, double *lse, int threads)
+{
+    return oracle_attention_f64_ex(q, k, v, B, H, H, N, N, d, scale, rows, nrows,
+                                   o, lse, threads);
 }

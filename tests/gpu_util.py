@@ -97,3 +97,46 @@ def edge_rows(w, count: int) -> np.ndarray:
         fixed += [(0, 0, t - 1), (0, 0, t)]
     rows.append(np.array(fixed, dtype=np.int64))
     return np.concatenate(rows)
+
+
+def run_fa_ex(q, k, v, dtype: str, num_splits: int, scale=None, stream=None, with_lse=True):
+    """fa_fwd_ex through the C ABI on poisoned outputs, with a workspace the
+    caller (this test) allocates.  Returns (o, lse) as numpy."""
+    import torch
+    B, H, Nq, d = q.shape
+    H_kv, Nkv = k.shape[1], k.shape[2]
+    tq, tk, tv = (to_device(x, dtype) for x in (q, k, v))
+    o = torch.full_like(tq, float("nan"))
+    lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda") if with_lse else None
+    wbytes = fab.fa_fwd_ex_workspace_size(B, H, Nq, Nkv, d, num_splits)
+    ws = torch.full((max(wbytes, 16) // 4,), float("nan"), dtype=torch.float32, device="cuda")
+    s = stream if stream is not None else torch.cuda.current_stream()
+    dt = fab.FA_DTYPE_BF16 if dtype == "bf16" else fab.FA_DTYPE_F32
+    sc = float(I.default_scale(d) if scale is None else scale)
+    st = fab.fa_fwd_ex(tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), o.data_ptr(),
+                       lse.data_ptr() if lse is not None else None, B, H, H_kv, Nq, Nkv, d, sc, dt,
+                       num_splits, ws.data_ptr() if wbytes else None, wbytes, s.cuda_stream)
+    assert st == fab.FA_OK, (st, fab.fa_status_string(st), fab.fa_last_error_message())
+    st = fab.fa_device_status(s.cuda_stream)
+    assert st == fab.FA_OK, (st, fab.fa_status_string(st), fab.fa_last_error_message())
+    return o.float().cpu().numpy(), (lse.cpu().numpy() if lse is not None else None)
+
+
+def compare_ex(dtype: str, o_gpu, lse_gpu, q, k, v, scale=None, rows=None):
+    d = q.shape[3]
+    sc = float(I.default_scale(d) if scale is None else scale)
+    if rows is None:
+        o_ref, l_ref = oracle.attention_f64_ex(q, k, v, sc)
+        og, lg = o_gpu, lse_gpu
+    else:
+        rows = np.asarray(rows, dtype=np.int64)
+        o_ref, l_ref = oracle.attention_f64_ex(q, k, v, sc, rows=rows)
+        og = o_gpu[rows[:, 0], rows[:, 1], rows[:, 2]]
+        lg = lse_gpu[rows[:, 0], rows[:, 1], rows[:, 2]] if lse_gpu is not None else None
+    err_o = float(np.max(np.abs(og.astype(np.float64) - o_ref) - o_allowance(o_ref, dtype)))
+    err_l = float(np.max(np.abs(lg.astype(np.float64) - l_ref))) if lg is not None else 0.0
+    return err_o, err_l
+
+
+def tol_o_dtype(dtype: str) -> float:
+    return TOL_O_BF16 if dtype == "bf16" else TOL_O_F32

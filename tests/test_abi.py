@@ -98,3 +98,37 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(fab, "_lib", None)
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         fab.load(str(tmp_path / "absent.so"))
+
+
+def validate_ex(q=Q, k=K, v=V, o=O, lse=L, B=2, H=8, H_kv=2, Nq=1, Nkv=4096, d=128, scale=0.088,
+                dtype=fab.FA_DTYPE_BF16, splits=1, ws=None, wbytes=0):
+    return fab.fa_fwd_ex_validate(q, k, v, o, lse, B, H, H_kv, Nq, Nkv, d, scale, dtype, splits, ws,
+                                  wbytes)
+
+
+def test_ex_validation(lib):
+    WS = 6 << 32
+    assert validate_ex() == fab.FA_OK
+    assert validate_ex(H_kv=3) == fab.FA_ERR_INVALID_ARG          # 8 query heads, 3 kv heads
+    assert validate_ex(H_kv=0) == fab.FA_ERR_INVALID_ARG
+    assert validate_ex(Nq=0) == fab.FA_ERR_INVALID_ARG
+    assert validate_ex(splits=0) == fab.FA_ERR_INVALID_ARG
+    need = fab.fa_fwd_ex_workspace_size(2, 8, 1, 4096, 128, 8)
+    assert need == 8 * 2 * 8 * 1 * (128 + 4) * 4
+    assert validate_ex(splits=8) == fab.FA_ERR_INVALID_ARG          # workspace missing
+    assert validate_ex(splits=8, ws=WS, wbytes=need - 1) == fab.FA_ERR_INVALID_ARG
+    assert validate_ex(splits=8, ws=WS, wbytes=need) == fab.FA_OK
+    assert validate_ex(splits=8, ws=WS + 8, wbytes=need) == fab.FA_ERR_ALIGNMENT
+    assert validate_ex(splits=8, ws=O, wbytes=need) == fab.FA_ERR_INVALID_ARG  # overlaps o
+
+
+def test_split_planning(lib):
+    # capped at one partition per 128 keys and at 32
+    assert fab.fa_fwd_ex_workspace_size(1, 1, 10, 200, 64, 8) == 2 * 10 * 68 * 4
+    assert fab.fa_fwd_ex_workspace_size(1, 1, 10, 100, 64, 8) == 0
+    assert fab.fa_fwd_ex_workspace_size(1, 1, 10, 1 << 20, 64, 64) == 32 * 10 * 68 * 4
+    # no empty partition: 5 tiles in 4 requested -> 3 partitions of 2, 2, 1 tiles
+    assert fab.fa_fwd_ex_workspace_size(1, 1, 1, 5 * 128, 64, 4) == 3 * 1 * 68 * 4
+    assert fab.fa_fwd_ex_splits(1, 1, 512, 512, 152) == 4          # 2 CTAs; capped at 4 key tiles
+    assert fab.fa_fwd_ex_splits(2, 32, 8192, 8192, 152) == 1       # 2048 CTAs fill the GPU
+    assert fab.fa_fwd_ex_splits(2, 4, 1000, 1000, 152) == 4

@@ -1,0 +1,99 @@
+"""fa_fwd_ex on the GPU against the fp64 oracle: key-range partitions
+(split-KV) merged by the second kernel, query and key lengths that differ
+(decode steps: one query against a long key cache), and grouped key/value
+heads (GQA / MQA).  Same tolerances as the square parity tests."""
+import numpy as np
+import pytest
+
+from exact_tiled_attention_04_gb300 import binding as fab
+from exact_tiled_attention_04_gb300 import inputs as I
+
+from .gpu_util import TOL_LSE, compare_ex, ensure_library, run_fa_ex, tol_o_dtype
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return ensure_library()
+
+
+def check(dtype, q, k, v, splits, rows=None):
+    o, lse = run_fa_ex(q, k, v, dtype, splits)
+    if rows is None:
+        assert np.isfinite(o).all() and np.isfinite(lse).all()
+    err_o, err_l = compare_ex(dtype, o, lse, q, k, v, rows=rows)
+    assert err_o <= tol_o_dtype(dtype), (q.shape, k.shape, splits, err_o)
+    assert err_l <= TOL_LSE, (q.shape, k.shape, splits, err_l)
+    return o, lse
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 8, 32])
+@pytest.mark.parametrize("d", [64, 128])
+def test_split_kv_bf16(splits, d):
+    q, k, v = I.make_general(1, 2, 2, 300, 1000, d, "bf16", seed=50 + splits)
+    check("bf16", q, k, v, splits)
+
+
+@pytest.mark.parametrize("splits", [1, 4])
+def test_split_kv_f32(splits):
+    q, k, v = I.make_general(1, 2, 2, 200, 700, 64, "f32", seed=60 + splits)
+    check("f32", q, k, v, splits)
+
+
+@pytest.mark.parametrize("Nkv", [1, 127, 128, 4097])
+@pytest.mark.parametrize("splits", [1, 16])
+def test_decode_single_query(Nkv, splits):
+    q, k, v = I.make_general(2, 8, 8, 1, Nkv, 128, "bf16", seed=70 + Nkv)
+    check("bf16", q, k, v, splits)
+
+
+@pytest.mark.parametrize("H,H_kv", [(8, 2), (8, 1), (6, 3)])
+def test_grouped_kv_heads(H, H_kv):
+    q, k, v = I.make_general(2, H, H_kv, 257, 511, 64, "bf16", seed=80 + H_kv)
+    check("bf16", q, k, v, 1)
+    check("bf16", q, k, v, 4)
+
+
+def test_gqa_decode_long_cache():
+    """A decode step of a grouped-query model against a 16k-key cache, split
+    across 32 partitions; checked on every (b, h) row."""
+    q, k, v = I.make_general(4, 32, 8, 1, 16384, 128, "bf16", seed=90)
+    check("bf16", q, k, v, 32)
+
+
+def test_more_queries_than_keys():
+    q, k, v = I.make_general(1, 3, 3, 1000, 130, 128, "bf16", seed=91)
+    check("bf16", q, k, v, 2)
+
+
+def test_split_matches_unsplit_closely():
+    q, k, v = I.make_general(2, 4, 4, 512, 2048, 128, "bf16", seed=92)
+    o1, l1 = run_fa_ex(q, k, v, "bf16", 1)
+    o8, l8 = run_fa_ex(q, k, v, "bf16", 8)
+    assert np.max(np.abs(o1 - o8)) <= 2 ** -7 and np.max(np.abs(l1 - l8)) <= 1e-4
+
+
+def test_fa_fwd_equals_fa_fwd_ex_unsplit():
+    w = I.custom(2, 3, 333, 128, "bf16", seed=93)
+    q, k, v = I.make(w)
+    from .gpu_util import run_fa
+    o_a, l_a = run_fa(w, q, k, v)
+    o_b, l_b = run_fa_ex(q, k, v, "bf16", 1)
+    assert np.array_equal(o_a, o_b) and np.array_equal(l_a, l_b)
+
+
+def test_workspace_too_small_is_rejected():
+    q, k, v = I.make_general(1, 2, 2, 64, 1024, 64, "bf16", seed=94)
+    need = fab.fa_fwd_ex_workspace_size(1, 2, 64, 1024, 64, 4)
+    assert need == 4 * 1 * 2 * 64 * (64 + 4) * 4
+    from .gpu_util import to_device
+    tq, tk, tv = (to_device(x, "bf16") for x in (q, k, v))
+    o = torch.empty_like(tq)
+    ws = torch.empty(need // 4, dtype=torch.float32, device="cuda")
+    st = fab.fa_fwd_ex(tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), o.data_ptr(), None, 1, 2, 2, 64,
+                       1024, 64, 0.125, fab.FA_DTYPE_BF16, 4, ws.data_ptr(), need - 16, None)
+    assert st == fab.FA_ERR_INVALID_ARG

@@ -199,9 +199,44 @@ def pin_online_tile_splits(lib):
             assert np.max(np.abs(ll - lse[0, 0])) <= 1e-12, (trial, deferred)
 
 
+def pin_general_shapes_sdpa(lib):
+    """Grouped key/value heads and different query / key lengths against
+    PyTorch SDPA with the key/value heads repeated explicitly (query head h
+    uses key/value head h // group)."""
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    for (B, H, H_kv, Nq, Nkv, d, scale) in [(2, 6, 3, 37, 53, 24, 0.4), (1, 4, 1, 1, 130, 16, 0.25),
+                                             (1, 2, 2, 70, 9, 8, 1.1)]:
+        q, k, v = rand(B, H, Nq, d), rand(B, H_kv, Nkv, d), rand(B, H_kv, Nkv, d)
+        o, lse = oracle.attention_f64_ex(q, k, v, scale, lib=lib)
+        tq, tk, tv = (torch.from_numpy(x.astype(np.float64)) for x in (q, k, v))
+        g = H // H_kv
+        tk, tv = tk.repeat_interleave(g, dim=1), tv.repeat_interleave(g, dim=1)
+        ref = F.scaled_dot_product_attention(tq, tk, tv, scale=float(scale)).numpy()
+        assert np.max(np.abs(o - ref)) <= 1e-12
+        ref_lse = torch.logsumexp(float(scale) * tq @ tk.transpose(-1, -2), dim=-1).numpy()
+        assert np.max(np.abs(lse - ref_lse)) <= 1e-12
+
+
+def pin_decode_row_materialised(lib):
+    """One query against many keys (a decode step) equals the materialised
+    softmax of its score row (SciPy), for every query head of a grouped layout."""
+    from scipy.special import logsumexp, softmax
+    B, H, H_kv, Nkv, d, scale = 2, 8, 2, 300, 32, 0.17
+    q, k, v = rand(B, H, 1, d), rand(B, H_kv, Nkv, d), rand(B, H_kv, Nkv, d)
+    o, lse = oracle.attention_f64_ex(q, k, v, scale, lib=lib)
+    for b in range(B):
+        for h in range(H):
+            kk = k[b, h // (H // H_kv)].astype(np.float64)
+            vv = v[b, h // (H // H_kv)].astype(np.float64)
+            srow = scale * (kk @ q[b, h, 0].astype(np.float64))
+            assert np.max(np.abs(o[b, h, 0] - softmax(srow) @ vv)) <= 1e-12
+            assert abs(lse[b, h, 0] - logsumexp(srow)) <= 1e-12
+
+
 ALL_PINS = [pin_weights_sum_to_one, pin_identical_keys, pin_single_key, pin_zero_scale,
             pin_dominant_score, pin_bounds, pin_torch_sdpa, pin_materialised_scipy,
-            pin_online_tile_splits]
+            pin_online_tile_splits, pin_general_shapes_sdpa, pin_decode_row_materialised]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -253,6 +288,8 @@ def test_bad_arguments_rejected(oracle_lib):
         oracle.attention_f64(q, q, q, 1.0, rows=[(0, 0, 4)])
     with pytest.raises(ValueError):
         oracle.attention_f64(q, q, q[:, :, :3], 1.0)
+    with pytest.raises(ValueError):  # 3 query heads cannot share 2 key/value heads
+        oracle.attention_f64_ex(rand(1, 3, 4, 4), rand(1, 2, 5, 4), rand(1, 2, 5, 4), 1.0)
 
 
 def test_nan_input_propagates(oracle_lib):
