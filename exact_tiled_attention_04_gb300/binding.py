@@ -86,6 +86,11 @@ def load(path: str | None = None):
         lib.fa_fwd_ex_workspace_size.argtypes = [i64, i64, i64, i64, i64, c_int]
         lib.fa_fwd_ex_splits.restype = c_int
         lib.fa_fwd_ex_splits.argtypes = [i64, i64, i64, i64, c_int]
+        lib.fa_fwd_ex_static.restype = c_int
+        lib.fa_fwd_ex_static.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, c_int,
+                                         c_int, vp]
+        lib.fa_fwd_ex_static_capacity.restype = sz
+        lib.fa_fwd_ex_static_capacity.argtypes = []
         _lib = lib
         return lib
 
@@ -129,6 +134,19 @@ def fa_fwd_ex_workspace_size(B: int, H: int, N_q: int, N_kv: int, d: int, num_sp
 
 def fa_fwd_ex_splits(B: int, H: int, N_q: int, N_kv: int, num_sms: int) -> int:
     return int(load().fa_fwd_ex_splits(B, H, N_q, N_kv, num_sms))
+
+
+def fa_fwd_ex_static(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, H_kv: int,
+                     N_q: int, N_kv: int, d: int, scale: float, dtype: int, num_splits: int,
+                     stream: int | None) -> int:
+    """fa_fwd_ex for callers that cannot allocate device memory: the split
+    partials live in the library's static per-device array (see include/fa.h)."""
+    return load().fa_fwd_ex_static(q, k, v, o, lse or None, B, H, H_kv, N_q, N_kv, d, scale, dtype,
+                                   num_splits, stream or None)
+
+
+def fa_fwd_ex_static_capacity() -> int:
+    return int(load().fa_fwd_ex_static_capacity())
 
 
 def fa_device_status(stream: int | None) -> int:

@@ -369,3 +369,88 @@ int fa_selftest_barrier_timeout(void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of fa_fwd_ex.
+//
+// Some callers cannot obtain device scratch memory for the split-KV partials:
+// plugins inside inference engines that own the whole device memory pool,
+// and per-step code that must not call cudaMalloc (it can synchronise the
+// device and can fail at run time).  For them, the partials live in one
+// fixed array of device memory that belongs to this library: every GPU that
+// loads the library holds kStaticWorkspaceBytes until the process exits.
+// All calls on a device share the array and it keeps the last call's
+// contents; nothing in it needs to start at zero (every partial slot a call
+// reads was written earlier by the same call).  Calls whose kernels overlap
+// on the GPU (different streams, or host threads) race on the array and
+// must be serialised by the caller.
+namespace {
+
+constexpr size_t kStaticWorkspaceBytes = size_t(32) << 20;  // 32 MiB per device
+static __device__ __align__(256) unsigned char g_fa_static_workspace[kStaticWorkspaceBytes];
+
+void* g_static_ws[kMaxDevices] = {};
+std::mutex g_static_ws_mutex;
+
+// Device address of the static array on the current device, looked up once
+// per device (host code cannot use the array's name as a device address).
+void* static_workspace(int* status) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        set_error("cudaGetDevice", static_cast<int>(e), cudaGetErrorString(e));
+        *status = FA_ERR_CUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_static_ws_mutex);
+    if (g_static_ws[dev] == nullptr) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_fa_static_workspace);
+        if (e != cudaSuccess || ptr == nullptr) {
+            set_error("cudaGetSymbolAddress(static workspace)", static_cast<int>(e),
+                      cudaGetErrorString(e));
+            *status = FA_ERR_CUDA;
+            return nullptr;
+        }
+        g_static_ws[dev] = ptr;
+    }
+    *status = FA_OK;
+    return g_static_ws[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_fwd_ex_static_capacity(void) { return kStaticWorkspaceBytes; }
+
+int fa_fwd_ex_static(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                     int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d, float scale,
+                     int dtype, int num_splits, void* stream) {
+    if (B >= 1 && H >= 1 && N_q >= 1 && N_kv >= 1 && d >= 1 && num_splits >= 1) {
+        const size_t need = fa_fwd_ex_workspace_size(B, H, N_q, N_kv, d, num_splits);
+        if (need > kStaticWorkspaceBytes) {
+            std::snprintf(g_last_error, sizeof(g_last_error),
+                          "fa_fwd_ex_static: the split partials need %zu bytes, more than the "
+                          "%zu-byte static workspace; use fewer splits or fa_fwd_ex",
+                          need, kStaticWorkspaceBytes);
+            return FA_ERR_UNSUPPORTED;
+        }
+    }
+    // Host checks first.  A launch that keeps more than one partition fails
+    // them only for want of a workspace: check again with the static array
+    // once its device address is known.
+    int st = validate_ex(q, k, v, o, lse, B, H, H_kv, N_q, N_kv, d, scale, dtype, num_splits, nullptr,
+                         0);
+    void* ws = nullptr;
+    if (st == FA_ERR_INVALID_ARG && num_splits > 1) {
+        ws = static_workspace(&st);
+        if (st != FA_OK) return st;
+        st = validate_ex(q, k, v, o, lse, B, H, H_kv, N_q, N_kv, d, scale, dtype, num_splits, ws,
+                         kStaticWorkspaceBytes);
+    }
+    if (st != FA_OK) return st;
+    return launch_ex(q, k, v, o, lse, B, H, H_kv, N_q, N_kv, d, scale, dtype, num_splits, ws, stream);
+}
+
+}  // extern "C"

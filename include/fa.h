@@ -133,6 +133,35 @@ size_t fa_fwd_ex_workspace_size(int64_t B, int64_t H, int64_t N_q, int64_t N_kv,
 int fa_fwd_ex_splits(int64_t B, int64_t H, int64_t N_q, int64_t N_kv, int num_sms);
 
 /*
+ * fa_fwd_ex_static — fa_fwd_ex for callers that cannot allocate device
+ * memory (plugins of engines that own the whole device memory pool, or
+ * per-step code that must not call cudaMalloc, which can synchronise the
+ * device and can fail at run time).  Same arguments and results as
+ * fa_fwd_ex without the workspace: the split partials go to one static
+ * device array of fa_fwd_ex_static_capacity() bytes (32 MiB) that the library
+ * holds on every GPU that loads it, until the process exits.  The library
+ * allocates nothing.
+ *
+ *   - Sizes whose partials exceed the capacity return FA_ERR_UNSUPPORTED
+ *     (fa_fwd_ex_workspace_size() gives the bytes a call needs).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the array, which keeps the last call's
+ *     contents (nothing in it needs to start at zero).  Calls whose kernels
+ *     may overlap on the GPU race on it: serialise them.
+ *
+ * The pages have no counterpart of this entry point.
+ */
+int fa_fwd_ex_static(const void* q, const void* k, const void* v, void* o,
+                     float* lse, int64_t B, int64_t H, int64_t H_kv,
+                     int64_t N_q, int64_t N_kv, int64_t d, float scale,
+                     int dtype, int num_splits, void* stream);
+
+/* Bytes of the static array fa_fwd_ex_static uses, per device. */
+size_t fa_fwd_ex_static_capacity(void);
+
+/*
  * fa_device_status — synchronise `stream`, then read and clear the device
  * error word the kernels set when a bounded wait gives up.  Returns FA_OK,
  * FA_ERR_TIMEOUT, or FA_ERR_CUDA if the synchronisation itself failed.
