@@ -8,7 +8,7 @@ draws the seeded synthetic workloads.  Importing the package loads no CUDA
 code; the first call into ``binding`` loads the library and fails loudly if it
 was not built.
 """
-from .binding import (FA_DTYPE_BF16, FA_DTYPE_F32, FA_ERR_ALIGNMENT, FA_ERR_CUDA,  # noqa: F401
+from .binding import (FA_DTYPE_BF16, FA_DTYPE_F16, FA_DTYPE_F32, FA_FLAG_CAUSAL, FA_ERR_ALIGNMENT, FA_ERR_CUDA,  # noqa: F401
                       FA_ERR_INVALID_ARG, FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED, FA_OK, FAError,
                       attention, fa_device_status, fa_fwd, fa_fwd_ex, fa_fwd_ex_splits,
                       fa_fwd_ex_validate, fa_fwd_ex_workspace_size, fa_fwd_validate,

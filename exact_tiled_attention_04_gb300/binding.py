@@ -29,6 +29,8 @@ FA_ERR_CUDA = 4
 FA_ERR_TIMEOUT = 5
 FA_DTYPE_F32 = 0
 FA_DTYPE_BF16 = 1
+FA_DTYPE_F16 = 2
+FA_FLAG_CAUSAL = 0x100
 
 _lock = threading.Lock()
 _lib = None
@@ -174,13 +176,15 @@ def _dtype_code(t) -> int:
     import torch
     if t.dtype == torch.bfloat16:
         return FA_DTYPE_BF16
+    if t.dtype == torch.float16:
+        return FA_DTYPE_F16
     if t.dtype == torch.float32:
         return FA_DTYPE_F32
-    raise TypeError(f"unsupported dtype {t.dtype}: bfloat16 or float32")
+    raise TypeError(f"unsupported dtype {t.dtype}: bfloat16, float16 or float32")
 
 
 def attention(q, k, v, scale: float | None = None, out=None, lse=None, with_lse: bool = True,
-              stream=None):
+              stream=None, causal: bool = False):
     """O = softmax(scale * Q K^T) V for CUDA tensors [B, H, N, d].
 
     Returns (out, lse); lse is fp32 [B, H, N] (natural log) or None when
@@ -211,7 +215,7 @@ def attention(q, k, v, scale: float | None = None, out=None, lse=None, with_lse:
     with torch.cuda.device(q.device):
         st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                     lse.data_ptr() if lse is not None else None, B, H, N, d, float(scale),
-                    _dtype_code(q), s.cuda_stream)
+                    _dtype_code(q) | (FA_FLAG_CAUSAL if causal else 0), s.cuda_stream)
     if st != FA_OK:
         raise FAError(st, "fa_fwd")
     return out, lse

@@ -98,16 +98,17 @@ int encode_map(CUtensorMap* map, const void* base, int dtype, int64_t BH, int64_
                   static_cast<int>(g_encode_err), cudaGetErrorString(g_encode_err));
         return FA_ERR_CUDA;
     }
-    const cuuint64_t elem = dtype == FA_DTYPE_BF16 ? 2 : 4;
+    const cuuint64_t elem = dtype == FA_DTYPE_F32 ? 4 : 2;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                                 static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elem,
                                    static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * elem};
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem), 128, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map,
-                     dtype == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+    const CUtensorMapDataType type = dtype == FA_DTYPE_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                     : dtype == FA_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    CUresult r = enc(map, type,
                      3, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -172,15 +173,17 @@ size_t workspace_bytes_for(int64_t B, int64_t H, int64_t N_q, int64_t d, const S
 
 int validate_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
                 int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d,
-                float scale, int dtype, int num_splits, const void* workspace,
+                float scale, int dtype_arg, int num_splits, const void* workspace,
                 size_t workspace_bytes) {
     if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || H_kv < 1 || N_q < 1 || N_kv < 1 || d < 1) return FA_ERR_INVALID_ARG;
     if (H % H_kv != 0) return FA_ERR_INVALID_ARG;
     if (num_splits < 1) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
-    if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16) return FA_ERR_UNSUPPORTED;
-    if (dtype == FA_DTYPE_BF16 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (dtype_arg & ~(0xFF | FA_FLAG_CAUSAL)) return FA_ERR_INVALID_ARG;  // unknown flag
+    const int dtype = dtype_arg & 0xFF;
+    if (dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) return FA_ERR_UNSUPPORTED;
+    if (dtype != FA_DTYPE_F32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     if (dtype == FA_DTYPE_F32 && d != 64) return FA_ERR_UNSUPPORTED;
     // element counts and byte sizes must fit in int64 (d is 64 or 128 here)
     if (B > INT64_MAX / H) return FA_ERR_INVALID_ARG;
@@ -189,7 +192,7 @@ int validate_ex(const void* q, const void* k, const void* v, const void* o, cons
     if (BHkv > INT64_MAX / N_kv || BHkv * N_kv > INT64_MAX / (d * 4)) return FA_ERR_INVALID_ARG;
     // TMA coordinates are 32-bit; global strides below 2^40 bytes
     if (BH > kInt32Max || N_q > kInt32Max || N_kv > kInt32Max) return FA_ERR_UNSUPPORTED;
-    const int64_t elem = dtype == FA_DTYPE_BF16 ? 2 : 4;
+    const int64_t elem = dtype == FA_DTYPE_F32 ? 4 : 2;
     if (N_q * d * elem >= (int64_t(1) << 40) || N_kv * d * elem >= (int64_t(1) << 40))
         return FA_ERR_UNSUPPORTED;
     const SplitPlan sp = plan_splits(N_kv, num_splits);
@@ -223,8 +226,10 @@ int validate_ex(const void* q, const void* k, const void* v, const void* o, cons
 }
 
 int launch_ex(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
-              int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d, float scale, int dtype,
-              int num_splits, void* workspace, void* stream) {
+              int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d, float scale,
+              int dtype_arg, int num_splits, void* workspace, void* stream) {
+    const int dtype = dtype_arg & 0xFF;
+    const bool causal = (dtype_arg & FA_FLAG_CAUSAL) != 0;
     const int64_t BH = B * H;
     const SplitPlan sp = plan_splits(N_kv, num_splits);
     CUtensorMap mq, mk, mv, mo;
@@ -245,6 +250,8 @@ int launch_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     p.H = static_cast<int>(H);
     p.H_kv = static_cast<int>(H_kv);
     p.group = static_cast<int>(H / H_kv);
+    p.causal = causal ? 1 : 0;
+    p.causal_offset = static_cast<int>(N_kv - N_q);
     p.splits = sp.splits;
     p.tiles_per_split = sp.tiles_per_split;
     p.scale_log2 = scale * 1.4426950408889634f;
@@ -264,6 +271,10 @@ int launch_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
         e = fa::launch_fwd_bf16_d64(mq, mk, mv, mo, p, grid, s);
     else if (dtype == FA_DTYPE_BF16)
         e = fa::launch_fwd_bf16_d128(mq, mk, mv, mo, p, grid, s);
+    else if (dtype == FA_DTYPE_F16 && d == 64)
+        e = fa::launch_fwd_f16_d64(mq, mk, mv, mo, p, grid, s);
+    else if (dtype == FA_DTYPE_F16)
+        e = fa::launch_fwd_f16_d128(mq, mk, mv, mo, p, grid, s);
     else
         e = fa::launch_fwd_tf32_d64(mq, mk, mv, mo, p, grid, s);
     if (e == cudaSuccess && sp.splits > 1) {

@@ -73,7 +73,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
-template <bool TF32, int D>
+template <bool TF32, int D, bool F16 = false>
 struct FwdCfg {
     static constexpr int kElem = TF32 ? 4 : 2;
     static constexpr int kAtomElems = 128 / kElem;      // elements in one 128-byte swizzle row
@@ -89,7 +89,8 @@ struct FwdCfg {
     static constexpr int kKStages = TF32 ? 2 : (kTileBytes <= 16384 ? 4 : 3);
     static constexpr int kVStages = TF32 ? 2 : (kTileBytes <= 16384 ? 4 : 2);
     static constexpr int kVtAtomBytes = D * 128;  // V^T: D rows x 32 keys (128 bytes)
-    static constexpr uint32_t kFmt = TF32 ? 2u : 1u;
+    // instruction-descriptor operand format: 0 = fp16, 1 = bf16, 2 = tf32
+    static constexpr uint32_t kFmt = TF32 ? 2u : (F16 ? 0u : 1u);
     // S = Q K^T: M = 128, N = 128, A and B K-major.
     static constexpr uint32_t kIdescQK = instr_desc(kFmt, false, false, kTileM, kTileN);
     // O += P V: A (P) from TMEM, B (V) MN-major, M = 128.  bf16: one
@@ -204,7 +205,7 @@ __device__ __forceinline__ float row_extreme(const uint32_t (&s)[4][32]) {
 // (bf16 pairs in 32 columns, or TF32 values in 64 columns) and adds p (fp32)
 // into acc, per packed lane pair.  Pairs of keys go through the packed
 // f32x2 FMA / add.
-template <bool TF32, bool kMasked>
+template <bool TF32, bool F16, bool kMasked>
 __device__ __forceinline__ void exp_half(const uint32_t (&s)[4][32], uint64_t c2, uint64_t ns2,
                                          int valid, uint32_t tS, int h, uint64_t (&acc)[4]) {
     if constexpr (TF32) {
@@ -240,7 +241,7 @@ __device__ __forceinline__ void exp_half(const uint32_t (&s)[4][32], uint64_t c2
                 if (c0 >= valid) p0 = 0.0f;
                 if (c0 + 1 >= valid) p1 = 0.0f;
             }
-            const uint32_t pk = pack_bf16x2(p0, p1);
+            const uint32_t pk = pack_16x2<F16>(p0, p1);
             pw[i] = pk;
             acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
         }
@@ -399,12 +400,12 @@ __device__ void produce_tf32(const CUtensorMap& map_q, const CUtensorMap& map_k,
     }
 }
 
-template <bool TF32, int D>
+template <bool TF32, int D, bool F16 = false, bool kCausal = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
                   const FwdParams p) {
-    using C = FwdCfg<TF32, D>;
+    using C = FwdCfg<TF32, D, F16>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_u32 & 1023u)) & 1023u;
@@ -422,8 +423,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // query heads share one key/value head)
     const int kvh = (bh / p.H) * p.H_kv + (bh % p.H) / p.group;
     const int row0 = qb * 2 * kTileM;
+    // key tiles this query block can see: all, or under the causal mask
+    // those up to the last key its last row sees
+    int n_tiles_block = p.n_kv_tiles;
+    if (kCausal) {
+        const long long lim = min(static_cast<long long>(p.Nkv),
+                                  static_cast<long long>(row0) + 2 * kTileM + p.causal_offset);
+        n_tiles_block = lim <= 0 ? 0 : static_cast<int>((lim + kTileN - 1) / kTileN);
+    }
     const int t_begin = static_cast<int>(split) * p.tiles_per_split;
-    const int T = min(p.tiles_per_split, p.n_kv_tiles - t_begin);  // >= 1 (host guarantees)
+    // <= 0: this partition sees no key (causal mask); only its epilogue runs
+    const int T = min(p.tiles_per_split, n_tiles_block - t_begin);
+    const bool has_work = !kCausal || T > 0;  // without the mask every partition has a tile
 
     auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * static_cast<uint32_t>(i); };
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kOffAbort);
@@ -477,7 +488,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 8) {
         // warpgroup 2: TMA producer, tensor-core issuer, two idle warps
         regs_decrease<C::kOtherRegs>();
-      if (warp == kLoadWarp) {
+      if (!has_work) {
+        // no visible key: nothing to load or multiply
+      } else if (warp == kLoadWarp) {
         // ------------------------------------------------------ TMA producer
         if constexpr (TF32) {
             produce_tf32<D>(map_q, map_k, map_v, p, smem, sbase, lane, row0, bh, kvh, t_begin, T, abort_flag);
@@ -615,6 +628,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tO = tmem + lane_off + 256u + static_cast<uint32_t>(D * w);
         const float c = p.scale_log2;
 
+        // keys of this row's head visible to this row: all Nkv, or under the
+        // causal mask those up to i + causal_offset (may be none)
+        int row_limit = p.Nkv;
+        if (kCausal) {
+            const long long lim = static_cast<long long>(row0 + w * kTileM + t) + p.causal_offset + 1;
+            row_limit = static_cast<int>(max(-1ll, min(static_cast<long long>(p.Nkv), lim)));
+        }
         float m_ref = -INFINITY;  // reference maximum, base-2 scaled units
         float l = 0.0f;           // running sum of the weights p (fp32): gives lse
         float lq = 0.0f;          // running sum used to normalise O: l with each
@@ -625,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // exponentials while the other tile's products occupy the tensor core
         // (see kTurnAfterHalf for how far the turns overlap).
         if (w == 1 && lane == 0) mbar_arrive(bar(C::kBarTurn + 0));
-        for (int j = 0; j < T; ++j) {
+        for (int j = 0; j < T; ++j) {  // T <= 0: no key tile
             bool got = wait_phase(bar(C::kBarSFull + w), j & 1, abort_flag, p, 10);
             ok = __all_sync(0xffffffffu, got);
             if (!ok) break;
@@ -640,8 +660,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q) tmem_ld_wait(s[q]);
 
-            const int valid = p.Nkv - (t_begin + j) * kTileN;  // keys of this tile inside the sequence
-            if (valid < kTileN) {
+            // keys of this tile visible to this row (<= 0: none, >= 128: all);
+            // masking is decided per warp (tcgen05.st is warp-collective)
+            const int valid = row_limit - (t_begin + j) * kTileN;
+            // (without the causal mask `valid` is the same for every row)
+            const bool masked = kCausal ? __any_sync(0xffffffffu, valid < kTileN) : (valid < kTileN);
+            if (masked) {
                 // keys past N: copy key 0's score so they cannot win the max;
                 // their weight is zeroed below
 #pragma unroll
@@ -653,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // tile maximum of t = s * c (c may be negative or zero)
             const float mx = (c >= 0.0f) ? row_extreme<true>(s) : row_extreme<false>(s);
-            const float m_tile = mx * c;
+            const float m_tile = (!kCausal || valid > 0) ? mx * c : -INFINITY;
             const float m_new = fmaxf(m_ref, m_tile);
             const bool need = m_new > m_ref + kRescaleThreshold;  // always true on the first tile
 
@@ -695,10 +719,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                if (valid < kTileN) {
-                    exp_half<TF32, true>(s, c2, ns2, valid, tS, h, acc);
+                if (masked) {
+                    exp_half<TF32, F16, true>(s, c2, ns2, valid, tS, h, acc);
                 } else {
-                    exp_half<TF32, false>(s, c2, ns2, valid, tS, h, acc);
+                    exp_half<TF32, F16, false>(s, c2, ns2, valid, tS, h, acc);
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -713,13 +737,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // row then enters the normalisation exactly as it entered O.
             const float tsum = sum8(acc);
             const float pmax = ex2(fmaf(mx, c, -shift));
-            const float pmax_r = TF32 ? u2f(round_tf32(pmax)) : u2f(pack_bf16x2(pmax, 0.0f) << 16);
+            const float pmax_r = TF32 ? u2f(round_tf32(pmax)) : widen_lo16<F16>(pack_16x2<F16>(pmax, 0.0f));
             l += tsum;
-            lq += tsum + (pmax_r - pmax);
+            lq += tsum + ((!kCausal || valid > 0) ? pmax_r - pmax : 0.0f);
         }
 
         // ------------------------------------------------------- epilogue
-        if (ok) {
+        if (ok && has_work) {
             bool got = wait_phase(bar(C::kBarOFull + w), 0, abort_flag, p, 11);
             ok = __all_sync(0xffffffffu, got);
         }
@@ -728,7 +752,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool split_mode = p.splits > 1;
         if (ok && split_mode) {
             tc_fence_after();
-            store_partial<D>(p, tO, row, m_ref, l, lq);
+            if (has_work) {
+                store_partial<D>(p, tO, row, m_ref, l, lq);
+            } else if (row < p.Nq) {
+                // an empty partition: weight 0 in the merge (its O slot is not read)
+                const size_t slab = static_cast<size_t>(gridDim.x / p.splits / p.n_q_blocks) * p.Nq;
+                const size_t r = split * slab + static_cast<size_t>(bh) * p.Nq + row;
+                *reinterpret_cast<float4*>(p.ml_part + r * 4) = make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
+            }
         }
         if (ok && !split_mode) {
             tc_fence_after();
@@ -736,8 +767,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t o[32];
-                tmem_ld32(tO + 32u * q, o);
-                tmem_ld_wait(o);
+                if (has_work) {
+                    tmem_ld32(tO + 32u * q, o);
+                    tmem_ld_wait(o);
+                } else {  // no visible key: O = 0 (and lse = -inf below)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
                 if constexpr (TF32) {
                     // 32 fp32 = one 128-byte swizzle row of atom q
                     uint8_t* rowp = stage + q * C::kAtomBytes + t * 128;
@@ -751,16 +787,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<uint4*>(rowp + ((ch ^ (t & 7)) << 4)) = v4;
                     }
                 } else {
-                    // 32 bf16 = half a swizzle row: chunks 4*(q%2) .. +3 of atom q/2
+                    // 32 bf16 / fp16 = half a swizzle row: chunks 4*(q%2) .. +3 of atom q/2
                     uint8_t* rowp = stage + (q / 2) * C::kAtomBytes + t * 128;
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
                         const int ch = (q % 2) * 4 + cc;
                         uint4 v4;
-                        v4.x = pack_bf16x2(u2f(o[8 * cc + 0]) * inv_l, u2f(o[8 * cc + 1]) * inv_l);
-                        v4.y = pack_bf16x2(u2f(o[8 * cc + 2]) * inv_l, u2f(o[8 * cc + 3]) * inv_l);
-                        v4.z = pack_bf16x2(u2f(o[8 * cc + 4]) * inv_l, u2f(o[8 * cc + 5]) * inv_l);
-                        v4.w = pack_bf16x2(u2f(o[8 * cc + 6]) * inv_l, u2f(o[8 * cc + 7]) * inv_l);
+                        v4.x = pack_16x2<F16>(u2f(o[8 * cc + 0]) * inv_l, u2f(o[8 * cc + 1]) * inv_l);
+                        v4.y = pack_16x2<F16>(u2f(o[8 * cc + 2]) * inv_l, u2f(o[8 * cc + 3]) * inv_l);
+                        v4.z = pack_16x2<F16>(u2f(o[8 * cc + 4]) * inv_l, u2f(o[8 * cc + 5]) * inv_l);
+                        v4.w = pack_16x2<F16>(u2f(o[8 * cc + 6]) * inv_l, u2f(o[8 * cc + 7]) * inv_l);
                         *reinterpret_cast<uint4*>(rowp + ((ch ^ (t & 7)) << 4)) = v4;
                     }
                 }
@@ -795,12 +831,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool TF32, int D>
-cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                       const CUtensorMap& o, const FwdParams& p, unsigned int grid,
-                       cudaStream_t stream) {
-    using C = FwdCfg<TF32, D>;
-    auto kern = fa_fwd_kernel<TF32, D>;
+template <bool TF32, int D, bool F16, bool kCausal>
+cudaError_t launch_fwd_variant(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               const CUtensorMap& o, const FwdParams& p, unsigned int grid,
+                               cudaStream_t stream) {
+    using C = FwdCfg<TF32, D, F16>;
+    auto kern = fa_fwd_kernel<TF32, D, F16, kCausal>;
     // The register split above relies on the compiled kernel holding exactly
     // kLaunchRegs per thread; refuse to launch otherwise (a setmaxnreg.inc
     // without the registers behind it would never return).
@@ -815,4 +851,16 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
     return cudaGetLastError();
 }
 
+}  // namespace fa
+
+namespace fa {
+// Causal and unmasked kernels are separate instantiations: the unmasked one
+// keeps a tile's key count uniform across rows.
+template <bool TF32, int D, bool F16 = false>
+cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                       const CUtensorMap& o, const FwdParams& p, unsigned int grid,
+                       cudaStream_t stream) {
+    return p.causal ? launch_fwd_variant<TF32, D, F16, true>(q, k, v, o, p, grid, stream)
+                    : launch_fwd_variant<TF32, D, F16, false>(q, k, v, o, p, grid, stream);
+}
 }  // namespace fa

@@ -26,6 +26,8 @@ struct FwdParams {
     int H;                   // query heads
     int group;               // query heads per key/value head (H / H_kv)
     int H_kv;                // key / value heads
+    int causal;              // 1: query i sees keys j <= i + causal_offset only
+    int causal_offset;       // Nkv - Nq (the last query sees every key)
     int splits;              // key-range partitions per query block (1 = none)
     int tiles_per_split;     // key tiles per partition
     float scale_log2;        // scale * log2(e)
@@ -67,6 +69,12 @@ cudaError_t launch_fwd_bf16_d64(const CUtensorMap& q, const CUtensorMap& k, cons
 cudaError_t launch_fwd_bf16_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                  const CUtensorMap& o, const FwdParams& p, unsigned int grid,
                                  cudaStream_t stream);
+cudaError_t launch_fwd_f16_d64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               const CUtensorMap& o, const FwdParams& p, unsigned int grid,
+                               cudaStream_t stream);
+cudaError_t launch_fwd_f16_d128(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                                const CUtensorMap& o, const FwdParams& p, unsigned int grid,
+                                cudaStream_t stream);
 cudaError_t launch_fwd_tf32_d64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                 const CUtensorMap& o, const FwdParams& p, unsigned int grid,
                                 cudaStream_t stream);

@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const MergeParams m) {
     for (int i = 0; i < kPer; ++i) acc[i] = 0.0f;
     for (int sp = 0; sp < m.splits; ++sp) {
         const float w = __shfl_sync(0xffffffffu, ws, sp);
+        if (w == 0.0f) continue;  // a partition with no visible key (its O slot is not written)
         const float* src = m.o_part + (static_cast<size_t>(sp) * slab + row) * D + lane * kPer;
         if constexpr (kPer == 4) {
             const float4 x = *reinterpret_cast<const float4*>(src);
@@ -69,10 +70,11 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const MergeParams m) {
     }
     const float inv = LQ > 0.0f ? 1.0f / LQ : 0.0f;
     const size_t out = static_cast<size_t>(row) * D + lane * kPer;
-    if constexpr (kDtype == FA_DTYPE_BF16) {
+    if constexpr (kDtype == FA_DTYPE_BF16 || kDtype == FA_DTYPE_F16) {
         uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(m.o) + out);
 #pragma unroll
-        for (int i = 0; i < kPer; i += 2) dst[i / 2] = pack_bf16x2(acc[i] * inv, acc[i + 1] * inv);
+        for (int i = 0; i < kPer; i += 2)
+            dst[i / 2] = pack_16x2<kDtype == FA_DTYPE_F16>(acc[i] * inv, acc[i + 1] * inv);
     } else {
         float* dst = static_cast<float*>(m.o) + out;
 #pragma unroll
@@ -90,6 +92,10 @@ cudaError_t launch_merge(const MergeParams& m, int d, int dtype, cudaStream_t st
         fa_merge_kernel<64, FA_DTYPE_BF16><<<blocks, 256, 0, stream>>>(m);
     else if (d == 64 && dtype == FA_DTYPE_F32)
         fa_merge_kernel<64, FA_DTYPE_F32><<<blocks, 256, 0, stream>>>(m);
+    else if (d == 128 && dtype == FA_DTYPE_F16)
+        fa_merge_kernel<128, FA_DTYPE_F16><<<blocks, 256, 0, stream>>>(m);
+    else if (d == 64 && dtype == FA_DTYPE_F16)
+        fa_merge_kernel<64, FA_DTYPE_F16><<<blocks, 256, 0, stream>>>(m);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();

@@ -231,6 +231,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
+// Two floats to a packed fp16x2 word, round to nearest even; `lo` in bits 0-15.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// The 16-bit half of a packed word in bits 0-15 widened to fp32 (bf16 or fp16).
+template <bool kF16>
+__device__ __forceinline__ float widen_lo16(uint32_t w) {
+    if constexpr (kF16) {
+        float f;
+        asm("{\n\t.reg .b16 h, l;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(w));
+        return f;
+    } else {
+        return __uint_as_float(w << 16);
+    }
+}
+// Pack two floats as the 16-bit type the products use (bf16 or fp16).
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack_16x2(float lo, float hi) {
+    if constexpr (kF16) return pack_f16x2(lo, hi);
+    else return pack_bf16x2(lo, hi);
+}
+
 // fp32 rounded to the nearest TF32 value (ties away), kept in a 32-bit word.
 __device__ __forceinline__ uint32_t round_tf32(float x) {
     uint32_t r;

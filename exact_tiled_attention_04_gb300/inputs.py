@@ -130,7 +130,7 @@ class Workload:
     H: int
     N: int
     d: int
-    dtype: str            # "bf16" or "f32": the kernel's input/output dtype
+    dtype: str            # "bf16", "f16" or "f32": the kernel's input/output dtype
     seed: int
     factor: float = 1.0   # multiplier applied to every drawn value
     identical_k_heads: tuple = ()      # (b, h): every K row equals that head's K row 0
@@ -184,15 +184,19 @@ def custom(B: int, H: int, N: int, d: int, dtype: str = "bf16", seed: int = 11,
 
 
 def _finish(values: np.ndarray, dtype: str) -> np.ndarray:
-    """float64 -> float32 (RNE) -> bfloat16 (RNE) for bf16 workloads, in
-    independent chunks on a thread pool."""
+    """float64 -> float32 (RNE) -> bfloat16 or float16 (RNE) for bf16 / f16
+    workloads, in independent chunks on a thread pool."""
     flat = values.reshape(-1)
     out = np.empty(flat.shape, dtype=np.float32)
     step = 1 << 22
 
     def one(i0):
         x = flat[i0:i0 + step].astype(np.float32)
-        out[i0:i0 + step] = round_to_bf16(x) if dtype == "bf16" else x
+        if dtype == "bf16":
+            x = round_to_bf16(x)
+        elif dtype == "f16":
+            x = x.astype(np.float16).astype(np.float32)  # round to nearest even
+        out[i0:i0 + step] = x
 
     starts = list(range(0, flat.size, step))
     workers = max(1, min(len(starts), os.cpu_count() or 1, 32))

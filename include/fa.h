@@ -36,11 +36,23 @@ typedef enum {
     FA_ERR_TIMEOUT = 5       /* a kernel gave up waiting on an internal barrier (device status) */
 } fa_status_t;
 
-/* Element type of q, k, v and o. */
+/* Element type of q, k, v and o (the low 8 bits of every `dtype` argument). */
 typedef enum {
     FA_DTYPE_F32 = 0,   /* fp32 in/out; the two contractions run on TF32 tensor cores */
-    FA_DTYPE_BF16 = 1   /* bf16 in/out; fp32 accumulation and softmax */
+    FA_DTYPE_BF16 = 1,  /* bf16 in/out; fp32 accumulation and softmax */
+    FA_DTYPE_F16 = 2    /* fp16 in/out; fp32 accumulation and softmax */
 } fa_dtype_t;
+
+/*
+ * Flags OR-ed into a `dtype` argument.
+ *
+ * FA_FLAG_CAUSAL: autoregressive attention, query i sees only the keys
+ * j <= i + (N_kv - N_q) (N_q = N_kv: the usual lower-triangular mask; the
+ * last query always sees every key, as a decode step against a key cache
+ * does).  A query that sees no key (N_q > N_kv) gets O = 0 and lse = -inf.
+ * Causal masking is not on the pages; this is the conventional reading.
+ */
+#define FA_FLAG_CAUSAL 0x100
 
 /*
  * fa_fwd — enqueue the attention forward pass on `stream`.
@@ -51,9 +63,9 @@ typedef enum {
  *   lse     : device pointer, fp32 [B, H, N], natural-log units; may be NULL,
  *             which skips the store.
  *   B, H, N : batch, heads, sequence length (queries = keys = N), each >= 1.
- *   d       : head dimension: 64 or 128 for bf16, 64 for fp32.
+ *   d       : head dimension: 64 or 128 for bf16 and fp16, 64 for fp32.
  *   scale   : finite score scale (1/sqrt(d) for the pages' attention).
- *   dtype   : an fa_dtype_t value.
+ *   dtype   : an fa_dtype_t value, optionally OR FA_FLAG_CAUSAL.
  *   stream  : a cudaStream_t (NULL = the legacy default stream) on the
  *             current device; all pointers must be on that device.
  *

@@ -65,7 +65,7 @@ def _bind(path: str):
     lib.oracle_attention_f64_ex.argtypes = [
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
-        ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int64,
+        ctypes.c_int64, ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
     return lib
 
@@ -122,11 +122,14 @@ def attention_f64(q, k, v, scale: float, rows=None, threads: int = 0, lib=None):
     return o, lse
 
 
-def attention_f64_ex(q, k, v, scale: float, rows=None, threads: int = 0, lib=None):
+def attention_f64_ex(q, k, v, scale: float, rows=None, threads: int = 0, lib=None,
+                     causal: bool = False):
     """Exact attention in fp64, general shapes: q [B, H, Nq, d], k and v
     [B, H_kv, Nkv, d] with H_kv dividing H (query head h uses key/value head
-    h // (H // H_kv)).  Returns (o, lse): [B, H, Nq, d] and [B, H, Nq] for
-    rows=None, else [R, d] and [R] for the (b, h, i) triples in `rows`."""
+    h // (H // H_kv)).  causal: query i sees keys j <= i + (Nkv - Nq) only
+    (no visible key: O = 0, lse = -inf).  Returns (o, lse): [B, H, Nq, d] and
+    [B, H, Nq] for rows=None, else [R, d] and [R] for the (b, h, i) triples in
+    `rows`."""
     lib = lib or load()
     q = np.ascontiguousarray(q, dtype=np.float32)
     k = np.ascontiguousarray(k, dtype=np.float32)
@@ -144,8 +147,8 @@ def attention_f64_ex(q, k, v, scale: float, rows=None, threads: int = 0, lib=Non
     o = np.empty((nrows, d), dtype=np.float64)
     lse = np.empty((nrows,), dtype=np.float64)
     rc = lib.oracle_attention_f64_ex(q.ctypes.data, k.ctypes.data, v.ctypes.data, B, H, H_kv, Nq,
-                                     Nkv, d, float(scale), rows_ptr, nrows, o.ctypes.data,
-                                     lse.ctypes.data, int(threads))
+                                     Nkv, d, float(scale), int(bool(causal)), rows_ptr, nrows,
+                                     o.ctypes.data, lse.ctypes.data, int(threads))
     if rc != 0:
         raise ValueError(f"oracle_attention_f64_ex failed with status {rc}")
     if rows is None:

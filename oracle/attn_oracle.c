@@ -129,6 +129,7 @@ static void attention_row(const float *q_row, const float *k_head,
 typedef struct {
     const float *q, *k, *v;
     int64_t B, H, H_kv, Nq, N, d; /* N = key/value rows per head */
+    int causal;
     double scale;
     const int64_t *rows; /* nrows * 3 entries (b, h, i), or NULL = all */
     int64_t nrows;
@@ -160,8 +161,19 @@ static void *worker(void *arg)
         const int64_t kvh = b * jb->H_kv + h / (jb->H / jb->H_kv);
         const float *q_row = jb->q + ((b * jb->H + h) * jb->Nq + i) * jb->d;
         const int64_t kv_head = kvh * jb->N * jb->d;
+        /* causal: query i sees the keys j <= i + (Nkv - Nq), a prefix of the
+           key sequence; the other keys are excluded (weight 0) */
+        int64_t visible = jb->N;
+        if (jb->causal && i + (jb->N - jb->Nq) + 1 < visible)
+            visible = i + (jb->N - jb->Nq) + 1;
+        if (visible <= 0) { /* no visible key: O = 0, lse = -inf */
+            for (int64_t c = 0; c < jb->d; ++c)
+                jb->o[r * jb->d + c] = 0.0;
+            jb->lse[r] = -INFINITY;
+            continue;
+        }
         attention_row(q_row, jb->k + kv_head, jb->v + kv_head,
-                      jb->N, jb->d, jb->scale, s, jb->o + r * jb->d,
+                      visible, jb->d, jb->scale, s, jb->o + r * jb->d,
                       jb->lse + r);
     }
     free(s);
@@ -183,6 +195,11 @@ int oracle_default_threads(void)
  *   (Nq = 1: one decode step against Nkv cached keys, as in the FlashDecoding
  *   paragraph of "FlashAttention dissected", section "Interaction with the KV
  *   cache during inference").
+ *   causal  : 0, or 1 for autoregressive attention: query i sees only keys
+ *             j <= i + (Nkv - Nq) (the last query sees every key, as a decode
+ *             step against a key cache does); a query with no visible key
+ *             gets O = 0 and lse = -inf.  Not on the pages: the usual causal
+ *             reading of the KV-cache paragraph of "FlashAttention dissected".
  *   rows    : NULL for every row (output order b, h, i), else nrows triples
  *             (b, h, i); out-of-range triples return -1.
  *   o       : fp64 [nrows, d];  lse : fp64 [nrows]
@@ -191,7 +208,7 @@ int oracle_default_threads(void)
  */
 int oracle_attention_f64_ex(const float *q, const float *k, const float *v,
                             int64_t B, int64_t H, int64_t H_kv, int64_t Nq,
-                            int64_t Nkv, int64_t d, double scale,
+                            int64_t Nkv, int64_t d, double scale, int causal,
                             const int64_t *rows, int64_t nrows, double *o,
                             double *lse, int threads)
 {
@@ -227,6 +244,7 @@ int oracle_attention_f64_ex(const float *q, const float *k, const float *v,
         job_t *jb = &jobs[t];
         jb->q = q; jb->k = k; jb->v = v;
         jb->B = B; jb->H = H; jb->H_kv = H_kv; jb->Nq = Nq; jb->N = Nkv; jb->d = d;
+        jb->causal = causal;
         jb->scale = scale;
         jb->rows = rows;
         jb->nrows = nrows;
@@ -263,6 +281,6 @@ int oracle_attention_f64(const float *q, const float *k, const float *v,
                          double scale, const int64_t *rows, int64_t nrows,
                          double *o, double *lse, int threads)
 {
-    return oracle_attention_f64_ex(q, k, v, B, H, H, N, N, d, scale, rows, nrows,
+    return oracle_attention_f64_ex(q, k, v, B, H, H, N, N, d, scale, 0, rows, nrows,
                                    o, lse, threads);
 }

@@ -13,6 +13,12 @@ from exact_tiled_attention_04_gb300 import inputs as I
 TOL_O_BF16 = 1.5e-2
 TOL_O_F32 = 2e-3
 TOL_LSE = 1e-3
+# fp16 in/out (no stated bar): weights rounded to fp16 move O by at most
+# 2^-11 * 2 max|v| (about 2e-3 for |v| <= 4) and the output rounding by half
+# an fp16 ulp (<= 1e-3 for |O| < 2): 4e-3.
+TOL_O_F16 = 4e-3
+
+DTYPE_CODES = {"bf16": fab.FA_DTYPE_BF16, "f16": fab.FA_DTYPE_F16, "f32": fab.FA_DTYPE_F32}
 
 
 def ensure_library():
@@ -26,6 +32,8 @@ def to_device(x: np.ndarray, dtype: str):
     if dtype == "bf16":
         bits = I.bf16_bits(x).view(np.int16)
         return torch.from_numpy(bits).cuda().view(torch.bfloat16)
+    if dtype == "f16":
+        return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32).astype(np.float16)).cuda()
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
 
 
@@ -37,7 +45,7 @@ def run_fa(w, q, k, v, scale=None, with_lse=True, stream=None):
     o = torch.full_like(tq, float("nan"))
     lse = torch.full((w.B, w.H, w.N), float("nan"), dtype=torch.float32, device="cuda") if with_lse else None
     s = stream if stream is not None else torch.cuda.current_stream()
-    dt = fab.FA_DTYPE_BF16 if w.dtype == "bf16" else fab.FA_DTYPE_F32
+    dt = DTYPE_CODES[w.dtype]
     sc = float(w.scale if scale is None else scale)
     st = fab.fa_fwd(tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), o.data_ptr(),
                     lse.data_ptr() if lse is not None else None,
@@ -55,15 +63,23 @@ def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
     return np.ldexp(1.0, e - 9)
 
 
+def half_ulp_f16(x: np.ndarray) -> np.ndarray:
+    """Half an fp16 unit in the last place at |x| (11 significant bits)."""
+    _, e = np.frexp(np.abs(x))
+    return np.ldexp(1.0, e - 12)
+
+
 def o_allowance(x: np.ndarray, dtype: str) -> np.ndarray:
     """Extra error allowed on top of the absolute O tolerance.  A bf16 output
     is rounded to the nearest bf16 value, which alone can be off by half a
     bf16 ulp of |O|: 2^-6 = 0.0156 for |O| in [4, 8), more than the 1.5e-2
     bar.  Where that happens the bar becomes half an ulp plus 1e-3 of
     arithmetic error; everywhere else (|O| < 4) the bar is 1.5e-2 as stated."""
-    if dtype != "bf16":
-        return np.zeros_like(x)
-    return np.maximum(0.0, half_ulp_bf16(x) + 1e-3 - TOL_O_BF16)
+    if dtype == "bf16":
+        return np.maximum(0.0, half_ulp_bf16(x) + 1e-3 - TOL_O_BF16)
+    if dtype == "f16":
+        return np.maximum(0.0, half_ulp_f16(x) + 1e-3 - TOL_O_F16)
+    return np.zeros_like(x)
 
 
 def compare(w, o_gpu, lse_gpu, q, k, v, rows=None, scale=None):
@@ -85,7 +101,7 @@ def compare(w, o_gpu, lse_gpu, q, k, v, rows=None, scale=None):
 
 
 def tol_o(w) -> float:
-    return TOL_O_BF16 if w.dtype == "bf16" else TOL_O_F32
+    return tol_o_dtype(w.dtype)
 
 
 def edge_rows(w, count: int) -> np.ndarray:
@@ -99,7 +115,8 @@ def edge_rows(w, count: int) -> np.ndarray:
     return np.concatenate(rows)
 
 
-def run_fa_ex(q, k, v, dtype: str, num_splits: int, scale=None, stream=None, with_lse=True):
+def run_fa_ex(q, k, v, dtype: str, num_splits: int, scale=None, stream=None, with_lse=True,
+              causal=False):
     """fa_fwd_ex through the C ABI on poisoned outputs, with a workspace the
     caller (this test) allocates.  Returns (o, lse) as numpy."""
     import torch
@@ -111,7 +128,7 @@ def run_fa_ex(q, k, v, dtype: str, num_splits: int, scale=None, stream=None, wit
     wbytes = fab.fa_fwd_ex_workspace_size(B, H, Nq, Nkv, d, num_splits)
     ws = torch.full((max(wbytes, 16) // 4,), float("nan"), dtype=torch.float32, device="cuda")
     s = stream if stream is not None else torch.cuda.current_stream()
-    dt = fab.FA_DTYPE_BF16 if dtype == "bf16" else fab.FA_DTYPE_F32
+    dt = DTYPE_CODES[dtype] | (fab.FA_FLAG_CAUSAL if causal else 0)
     sc = float(I.default_scale(d) if scale is None else scale)
     st = fab.fa_fwd_ex(tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), o.data_ptr(),
                        lse.data_ptr() if lse is not None else None, B, H, H_kv, Nq, Nkv, d, sc, dt,
@@ -122,21 +139,29 @@ def run_fa_ex(q, k, v, dtype: str, num_splits: int, scale=None, stream=None, wit
     return o.float().cpu().numpy(), (lse.cpu().numpy() if lse is not None else None)
 
 
-def compare_ex(dtype: str, o_gpu, lse_gpu, q, k, v, scale=None, rows=None):
+def compare_ex(dtype: str, o_gpu, lse_gpu, q, k, v, scale=None, rows=None, causal=False):
+    """Max |GPU - oracle| (O with the rounding allowance, lse).  Rows with no
+    visible key must have lse = -inf on both sides (inf is reported if not)."""
     d = q.shape[3]
     sc = float(I.default_scale(d) if scale is None else scale)
     if rows is None:
-        o_ref, l_ref = oracle.attention_f64_ex(q, k, v, sc)
+        o_ref, l_ref = oracle.attention_f64_ex(q, k, v, sc, causal=causal)
         og, lg = o_gpu, lse_gpu
     else:
         rows = np.asarray(rows, dtype=np.int64)
-        o_ref, l_ref = oracle.attention_f64_ex(q, k, v, sc, rows=rows)
+        o_ref, l_ref = oracle.attention_f64_ex(q, k, v, sc, rows=rows, causal=causal)
         og = o_gpu[rows[:, 0], rows[:, 1], rows[:, 2]]
         lg = lse_gpu[rows[:, 0], rows[:, 1], rows[:, 2]] if lse_gpu is not None else None
     err_o = float(np.max(np.abs(og.astype(np.float64) - o_ref) - o_allowance(o_ref, dtype)))
-    err_l = float(np.max(np.abs(lg.astype(np.float64) - l_ref))) if lg is not None else 0.0
+    err_l = 0.0
+    if lg is not None:
+        lg = lg.astype(np.float64)
+        empty = np.isneginf(l_ref)
+        if not np.array_equal(empty, np.isneginf(lg)):
+            return err_o, float("inf")
+        err_l = float(np.max(np.abs(lg[~empty] - l_ref[~empty]))) if (~empty).any() else 0.0
     return err_o, err_l
 
 
 def tol_o_dtype(dtype: str) -> float:
-    return TOL_O_BF16 if dtype == "bf16" else TOL_O_F32
+    return {"bf16": TOL_O_BF16, "f16": TOL_O_F16, "f32": TOL_O_F32}[dtype]

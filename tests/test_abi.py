@@ -132,3 +132,12 @@ def test_split_planning(lib):
     assert fab.fa_fwd_ex_splits(1, 1, 512, 512, 152) == 4          # 2 CTAs; capped at 4 key tiles
     assert fab.fa_fwd_ex_splits(2, 32, 8192, 8192, 152) == 1       # 2048 CTAs fill the GPU
     assert fab.fa_fwd_ex_splits(2, 4, 1000, 1000, 152) == 4
+
+
+def test_dtype_flags(lib):
+    assert validate(dtype=fab.FA_DTYPE_F16) == fab.FA_OK
+    assert validate(dtype=fab.FA_DTYPE_F16, d=128) == fab.FA_OK
+    assert validate(dtype=fab.FA_DTYPE_F16, d=96) == fab.FA_ERR_UNSUPPORTED
+    assert validate(dtype=fab.FA_DTYPE_BF16 | fab.FA_FLAG_CAUSAL) == fab.FA_OK
+    assert validate(dtype=fab.FA_DTYPE_BF16 | 0x200) == fab.FA_ERR_INVALID_ARG  # unknown flag
+    assert validate_ex(dtype=fab.FA_DTYPE_F16 | fab.FA_FLAG_CAUSAL) == fab.FA_OK

@@ -234,9 +234,42 @@ def pin_decode_row_materialised(lib):
             assert abs(lse[b, h, 0] - logsumexp(srow)) <= 1e-12
 
 
+def pin_causal_sdpa(lib):
+    """Causal attention against PyTorch SDPA with an explicit boolean mask
+    built independently (key j visible to query i iff j <= i + Nkv - Nq),
+    with query and key lengths equal and different, and grouped heads."""
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    for (B, H, H_kv, Nq, Nkv, d, scale) in [(1, 2, 2, 40, 40, 16, 0.3), (2, 4, 2, 17, 60, 8, 0.7),
+                                             (1, 2, 1, 1, 33, 8, 0.5)]:
+        q, k, v = rand(B, H, Nq, d), rand(B, H_kv, Nkv, d), rand(B, H_kv, Nkv, d)
+        o, lse = oracle.attention_f64_ex(q, k, v, scale, lib=lib, causal=True)
+        tq, tk, tv = (torch.from_numpy(x.astype(np.float64)) for x in (q, k, v))
+        g = H // H_kv
+        tk, tv = tk.repeat_interleave(g, dim=1), tv.repeat_interleave(g, dim=1)
+        mask = torch.ones(Nq, Nkv, dtype=torch.bool).tril(diagonal=Nkv - Nq)
+        ref = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=float(scale)).numpy()
+        assert np.max(np.abs(o - ref)) <= 1e-12
+        sc = (float(scale) * tq @ tk.transpose(-1, -2)).masked_fill(~mask, float("-inf"))
+        assert np.max(np.abs(lse - torch.logsumexp(sc, dim=-1).numpy())) <= 1e-12
+
+
+def pin_causal_first_row_and_full_row(lib):
+    """Square causal attention: the first query sees only key 0 (O = v_0,
+    lse = s_00); the last query sees every key (equals the unmasked row)."""
+    N, d, scale = 50, 8, 0.6
+    q, k, v = rand(1, 1, N, d), rand(1, 1, N, d), rand(1, 1, N, d)
+    oc, lc = oracle.attention_f64_ex(q, k, v, scale, lib=lib, causal=True)
+    of, lf = oracle.attention_f64_ex(q, k, v, scale, lib=lib, causal=False)
+    assert np.array_equal(oc[0, 0, 0], v[0, 0, 0].astype(np.float64))
+    assert abs(lc[0, 0, 0] - scale * float(q[0, 0, 0].astype(np.float64) @ k[0, 0, 0].astype(np.float64))) <= 1e-13
+    assert np.max(np.abs(oc[0, 0, -1] - of[0, 0, -1])) == 0.0 and lc[0, 0, -1] == lf[0, 0, -1]
+
+
 ALL_PINS = [pin_weights_sum_to_one, pin_identical_keys, pin_single_key, pin_zero_scale,
             pin_dominant_score, pin_bounds, pin_torch_sdpa, pin_materialised_scipy,
-            pin_online_tile_splits, pin_general_shapes_sdpa, pin_decode_row_materialised]
+            pin_online_tile_splits, pin_general_shapes_sdpa, pin_decode_row_materialised,
+            pin_causal_sdpa, pin_causal_first_row_and_full_row]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -331,3 +364,11 @@ def test_pins_catch_planted_mistakes(mutant, tmp_path):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"mutant {mutant} passed every pin"
+
+
+def test_causal_query_without_visible_key(oracle_lib):
+    """More queries than keys: the first Nq - Nkv queries see no key."""
+    q, k, v = rand(1, 1, 10, 4), rand(1, 1, 6, 4), rand(1, 1, 6, 4)
+    o, lse = oracle.attention_f64_ex(q, k, v, 0.5, causal=True)
+    assert np.all(o[0, 0, :4] == 0.0) and np.all(np.isneginf(lse[0, 0, :4]))
+    assert np.all(np.isfinite(lse[0, 0, 4:]))
