@@ -44,6 +44,7 @@ if ROOT not in sys.path:
 METRIC = "attention fwd TFLOP/s (4·B·H·N²·d) on 1 GB300 and % of dense tensor peak"
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
 NOMINAL_TF32_OVER_BF16 = 0.5  # dense TF32 rate relative to dense bf16 (1.1 vs 2.25 PFLOP/s nominal)
 
 
@@ -192,15 +193,25 @@ def cpu_oracle_rate(w, q, k, v, target_s: float, max_rows: int | None = None):
     cores = oracle.default_threads()
     rows = I.sample_rows(w, 64, seed_offset=1000)
     t0 = time.perf_counter()
-    oracle.attention_f64(q, k, v, float(w.scale), rows=rows)
+    oracle.attention_f64_ex(q, k, v, float(w.scale), rows=rows, causal=w.causal)
     dt = max(time.perf_counter() - t0, 1e-6)
     n = int(64 * target_s / dt)
     n = max(cores, min(n, max_rows or n, w.B * w.H * w.N))
     rows = I.sample_rows(w, n, seed_offset=1001)
     t0 = time.perf_counter()
-    oracle.attention_f64(q, k, v, float(w.scale), rows=rows)
+    oracle.attention_f64_ex(q, k, v, float(w.scale), rows=rows, causal=w.causal)
     dt = time.perf_counter() - t0
-    return oracle.flops(w.B, w.H, w.N, w.d, rows=n) / dt / 1e12, cores, n, dt
+    return row_flops(w, rows) / dt / 1e12, cores, n, dt
+
+
+def row_flops(w, rows) -> float:
+    """Algorithmic flops of the given (b, h, i) query rows: 4 d per visible key."""
+    import numpy as np
+    i = np.asarray(rows)[:, 2].astype(np.float64)
+    visible = np.full_like(i, float(w.Nkv))
+    if w.causal:
+        visible = np.clip(i + (w.Nkv - w.N) + 1, 0, w.Nkv)
+    return float(4.0 * w.d * visible.sum())
 
 
 # ------------------------------------------------------------------- arms
@@ -217,16 +228,20 @@ def run_reference(args, w):
     budget_s = 150.0 / max(1, args.steps + args.warmup)
     rows = I.sample_rows(w, 16, seed_offset=2000)
     t0 = time.perf_counter()
-    oracle.attention_f64(q, k, v, float(w.scale), rows=rows)
+    oracle.attention_f64_ex(q, k, v, float(w.scale), rows=rows, causal=w.causal)
     per_row = max((time.perf_counter() - t0) / 16, 1e-7)
     n = int(max(1, min(4096, w.B * w.H * w.N, budget_s / per_row)))
     for i in range(args.warmup):
-        oracle.attention_f64(q, k, v, float(w.scale), rows=I.sample_rows(w, n, seed_offset=3000 + i))
+        oracle.attention_f64_ex(q, k, v, float(w.scale), rows=I.sample_rows(w, n, seed_offset=3000 + i),
+                                causal=w.causal)
+    total = 0.0
     t0 = time.perf_counter()
     for i in range(args.steps):
-        oracle.attention_f64(q, k, v, float(w.scale), rows=I.sample_rows(w, n, seed_offset=4000 + i))
+        rows = I.sample_rows(w, n, seed_offset=4000 + i)
+        oracle.attention_f64_ex(q, k, v, float(w.scale), rows=rows, causal=w.causal)
+        total += row_flops(w, rows)
     dt = time.perf_counter() - t0
-    value = oracle.flops(w.B, w.H, w.N, w.d, rows=n) * args.steps / dt / 1e12
+    value = total / dt / 1e12
     sample = f"{n} seeded query rows of the workload per step (of {w.B * w.H * w.N}), fp64, {cores} threads"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
@@ -241,13 +256,20 @@ def run_reference(args, w):
     return 0
 
 
-def config_of(w, n_gpus: int):
-    nbytes = 4 * w.B * w.H * w.N * w.d * (2 if w.dtype == "bf16" else 4) + 4 * w.B * w.H * w.N
+def config_of(w, n_gpus: int, splits: int = 1):
+    nbytes = w.bytes()
     l2 = (f"inputs larger than L2: q,k,v,o,lse = {nbytes / 1e6:.0f} MB per step (L2 129 MB), no flush"
           if nbytes > 129e6 else f"L2-resident: q,k,v,o,lse = {nbytes / 1e6:.1f} MB per step")
-    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype,
-            "inputs": f"seeded N(0,1) x {w.factor}", "scale": float(w.scale), "l2": l2,
-            "parallelism": f"independent replica per GPU x{n_gpus}"}
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype,
+           "inputs": f"seeded N(0,1) x {w.factor}", "scale": float(w.scale), "l2": l2,
+           "parallelism": f"independent replica per GPU x{n_gpus}"}
+    if w.general:
+        cfg.update({"H_kv": w.H_kv, "N_kv": w.Nkv})
+    if w.causal:
+        cfg["causal"] = True
+    if splits > 1:
+        cfg["splits"] = splits
+    return cfg
 
 
 def run_ours(args, w):
@@ -264,12 +286,15 @@ def run_ours(args, w):
 
     # per-rank inputs (weak scaling: every rank its own seeded copy)
     wr = I.Workload(w.name, w.B, w.H, w.N, w.d, w.dtype, w.seed + 17 * rank, w.factor,
-                    w.identical_k_heads, w.q_scaled_heads, w.oracle_rows, w.note)
+                    w.identical_k_heads, w.q_scaled_heads, w.oracle_rows, w.note, w.H_kv, w.Nkv,
+                    w.causal, w.splits)
     q, k, v = I.make(wr)
 
     def host_tensor(x):
         if w.dtype == "bf16":
             return torch.from_numpy(I.bf16_bits(x).view(np.int16)).view(torch.bfloat16)
+        if w.dtype == "f16":
+            return torch.from_numpy(np.ascontiguousarray(x, np.float32).astype(np.float16))
         return torch.from_numpy(np.ascontiguousarray(x, np.float32))
 
     hq, hk, hv = (host_tensor(x).pin_memory() for x in (q, k, v))
@@ -278,17 +303,27 @@ def run_ours(args, w):
     dlse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     sp = stream.cuda_stream
-    dt_code = fab.FA_DTYPE_BF16 if w.dtype == "bf16" else fab.FA_DTYPE_F32
+    dt_code = {"bf16": fab.FA_DTYPE_BF16, "f16": fab.FA_DTYPE_F16, "f32": fab.FA_DTYPE_F32}[w.dtype]
+    if w.causal:
+        dt_code |= fab.FA_FLAG_CAUSAL
     scale = float(w.scale)
+    splits = w.splits
+    if splits == 0:  # as many key partitions as fill one wave of SMs
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        splits = fab.fa_fwd_ex_splits(w.B, w.H, w.N, w.Nkv, sms)
+    wbytes = fab.fa_fwd_ex_workspace_size(w.B, w.H, w.N, w.Nkv, w.d, splits)
+    work = torch.empty(max(wbytes, 16), dtype=torch.uint8, device=dev)  # caller-owned scratch
+    kernels_per_step = 2 if wbytes else 1  # forward (+ merge of the partitions)
     launches = 0
 
     def step():
         nonlocal launches
-        st = fab.fa_fwd(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), do.data_ptr(), dlse.data_ptr(),
-                        w.B, w.H, w.N, w.d, scale, dt_code, sp)
+        st = fab.fa_fwd_ex(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), do.data_ptr(), dlse.data_ptr(),
+                           w.B, w.H, w.H_kv, w.N, w.Nkv, w.d, scale, dt_code, splits,
+                           work.data_ptr() if wbytes else None, wbytes, sp)
         if st != fab.FA_OK:
-            raise fab.FAError(st, "fa_fwd")
-        launches += 1
+            raise fab.FAError(st, "fa_fwd_ex")
+        launches += kernels_per_step
 
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
@@ -322,7 +357,7 @@ def run_ours(args, w):
     flops_rank = w.flops() * args.steps
     flops_all = reduce_sum(flops_rank, dist, dev)
     value = flops_all / (ms_total * 1e-3) / 1e12
-    kernel_ms = ms_local / args.steps  # one kernel per step on this stream
+    kernel_ms = ms_local / args.steps  # the step's kernels, all on this stream
     clk = clocks.summary()
 
     # ---- end to end: host copies inside the timed region
@@ -356,27 +391,43 @@ def run_ours(args, w):
 
     peaks = measured_peaks()
     bf16_peak = (peaks or {}).get("bf16_tflops")
+    hbm_peak = (peaks or {}).get("hbm_gbs")
     peak_note = "measured bf16 burst (MEASURED_PEAKS.json)"
     if not bf16_peak:
         bf16_peak, peak_note = FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16"
-    peak = bf16_peak if w.dtype == "bf16" else bf16_peak * NOMINAL_TF32_OVER_BF16
-    if w.dtype != "bf16":
+    if not hbm_peak:
+        hbm_peak = FALLBACK_HBM_GBS
+    tensor_peak = bf16_peak if w.dtype != "f32" else bf16_peak * NOMINAL_TF32_OVER_BF16
+    if w.dtype == "f32":
         peak_note += " x nominal tf32/bf16 ratio 0.5"
-    achieved = w.flops() / (kernel_ms * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                "frac": achieved / peak, "traffic": stored_traffic(w.name),
-                "kernel": f"fa_fwd_kernel<{'tf32' if w.dtype != 'bf16' else 'bf16'},{w.d}>",
-                "peak_source": peak_note,
-                "algorithmic_flops_per_launch": w.flops(),
-                "algorithmic_bytes_per_launch": 4 * w.B * w.H * w.N * w.d * (2 if w.dtype == "bf16" else 4)
-                + 4 * w.B * w.H * w.N}
+    elif w.dtype == "f16":
+        peak_note += " (fp16 and bf16 share the dense rate)"
+    step_s = kernel_ms * 1e-3
+    intensity = w.flops() / w.bytes()
+    ridge = tensor_peak * 1e12 / (hbm_peak * 1e9)
+    kernel_name = (f"fa_fwd_kernel<{w.dtype},{w.d}{',causal' if w.causal else ''}>"
+                   + (" + fa_merge_kernel" if kernels_per_step == 2 else ""))
+    if intensity >= ridge:
+        achieved = w.flops() / step_s / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": UNIT,
+                    "frac": achieved / tensor_peak, "peak_source": peak_note}
+    else:
+        achieved = w.bytes() / step_s / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": achieved / hbm_peak,
+                    "peak_source": "measured copy bandwidth (MEASURED_PEAKS.json)" if peaks else "fallback"}
+    roofline.update({"traffic": stored_traffic(w.name), "kernel": kernel_name,
+                     "algorithmic_flops_per_launch": w.flops(),
+                     "algorithmic_bytes_per_launch": w.bytes(),
+                     "arithmetic_intensity": intensity})
+    frac_tensor = value / world / tensor_peak
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": config_of(w, world),
-        "frac_of_peak": value / world / peak,
+        "config": config_of(w, world, splits),
+        "frac_of_peak": frac_tensor,
         "roofline": roofline,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},

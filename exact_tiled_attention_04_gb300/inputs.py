@@ -137,17 +137,46 @@ class Workload:
     q_scaled_heads: tuple = ()         # (b, h, factor): that head's Q drawn times factor
     oracle_rows: int | None = None     # compare on this many seeded rows (None = all)
     note: str = ""
+    H_kv: int = 0          # key/value heads (0: H, plain multi-head attention)
+    Nkv: int = 0           # key/value rows per head (0: N; N is the query rows)
+    causal: bool = False   # query i sees keys j <= i + Nkv - N only
+    splits: int = 1        # key-range partitions (0: as many as fill one wave)
     scale: np.float32 = field(init=False)
 
     def __post_init__(self):
         self.scale = default_scale(self.d)
+        self.H_kv = self.H_kv or self.H
+        self.Nkv = self.Nkv or self.N
 
     @property
     def shape(self):
         return (self.B, self.H, self.N, self.d)
 
+    @property
+    def kv_shape(self):
+        return (self.B, self.H_kv, self.Nkv, self.d)
+
+    @property
+    def general(self) -> bool:
+        return self.H_kv != self.H or self.Nkv != self.N
+
+    def visible_pairs(self) -> float:
+        """(query, key) pairs that carry weight, per (b, h)."""
+        if not self.causal:
+            return float(self.N) * float(self.Nkv)
+        off = self.Nkv - self.N
+        i = np.arange(self.N, dtype=np.float64)
+        return float(np.clip(i + off + 1, 0, self.Nkv).sum())
+
     def flops(self) -> float:
-        return 4.0 * self.B * self.H * self.N * self.N * self.d
+        """4 d flops per visible (query, key) pair: 4*B*H*N^2*d unmasked."""
+        return 4.0 * self.B * self.H * self.visible_pairs() * self.d
+
+    def bytes(self) -> float:
+        """Algorithmic bytes: read q, k, v once, write o and lse."""
+        elem = 4 if self.dtype == "f32" else 2
+        return (elem * self.d * (2 * self.B * self.H * self.N + 2 * self.B * self.H_kv * self.Nkv)
+                + 4 * self.B * self.H * self.N)
 
     def describe(self) -> str:
         return f"{self.name}: B={self.B} H={self.H} N={self.N} d={self.d} {self.dtype}"
@@ -155,10 +184,10 @@ class Workload:
 
 WORKLOADS = {
     "single_head_n512": Workload(
-        "single_head_n512", 1, 1, 512, 64, "f32", seed=1,
+        "single_head_n512", 1, 1, 512, 64, "f32", seed=1, splits=0,
         note="single head, fp32 inputs and output"),
     "tail_n1000": Workload(
-        "tail_n1000", 2, 4, 1000, 64, "bf16", seed=2,
+        "tail_n1000", 2, 4, 1000, 64, "bf16", seed=2, splits=0,
         identical_k_heads=((0, 1),), q_scaled_heads=((1, 2, 30.0),),
         note="N not a multiple of the tile; one head with identical keys, one with Q x30"),
     "b4h16_n2048": Workload("b4h16_n2048", 4, 16, 2048, 64, "bf16", seed=3),
@@ -174,6 +203,21 @@ WORKLOADS = {
 WORKLOADS["b1h32_n8192_d128"] = Workload(
     "b1h32_n8192_d128", 1, 32, 8192, 128, "bf16", seed=6, factor=0.5, oracle_rows=256,
     note="profiling case: half the headline shape")
+# Shapes of the next rows: a decode step of a grouped-query model against a
+# 16k-key cache (FlashDecoding: the keys split across the GPU), the headline
+# shape with 4:1 grouped key/value heads, with the causal mask, and in fp16.
+WORKLOADS["decode_b8h32kv8_n16384_d128"] = Workload(
+    "decode_b8h32kv8_n16384_d128", 8, 32, 1, 128, "bf16", seed=7, H_kv=8, Nkv=16384, splits=0,
+    note="one query per head against a 16k-key cache, grouped heads, split-KV")
+WORKLOADS["gqa_b2h32kv8_n8192_d128"] = Workload(
+    "gqa_b2h32kv8_n8192_d128", 2, 32, 8192, 128, "bf16", seed=8, factor=0.5, H_kv=8,
+    oracle_rows=256, note="headline shape, 4 query heads per key/value head")
+WORKLOADS["causal_b2h32_n8192_d128"] = Workload(
+    "causal_b2h32_n8192_d128", 2, 32, 8192, 128, "bf16", seed=9, factor=0.5, causal=True,
+    oracle_rows=256, note="headline shape, causal mask")
+WORKLOADS["f16_b2h32_n8192_d128"] = Workload(
+    "f16_b2h32_n8192_d128", 2, 32, 8192, 128, "f16", seed=10, factor=0.5, oracle_rows=256,
+    note="headline shape in fp16")
 HEADLINE = "b2h32_n8192_d128"
 SMALL = "single_head_n512"
 
@@ -210,7 +254,10 @@ def _finish(values: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def make(w: Workload):
-    """Return (q, k, v) float32 arrays [B, H, N, d] holding the rounded inputs."""
+    """Return (q, k, v) float32 arrays holding the rounded inputs: q
+    [B, H, N, d], k and v [B, H_kv, Nkv, d]."""
+    if w.general:
+        return make_general(w.B, w.H, w.H_kv, w.N, w.Nkv, w.d, w.dtype, w.seed, w.factor)
     n = w.B * w.H * w.N * w.d
     out = []
     for t in (TENSOR_Q, TENSOR_K, TENSOR_V):

@@ -97,3 +97,26 @@ def test_workspace_too_small_is_rejected():
     st = fab.fa_fwd_ex(tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), o.data_ptr(), None, 1, 2, 2, 64,
                        1024, 64, 0.125, fab.FA_DTYPE_BF16, 4, ws.data_ptr(), need - 16, None)
     assert st == fab.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name", ["single_head_n512", "tail_n1000", "decode_b8h32kv8_n16384_d128"])
+def test_workloads_in_bench_launch_configuration(name):
+    """The small workloads and the decode workload as the benchmark launches
+    them: fa_fwd_ex with the key partitions that fill one wave of SMs."""
+    w = I.WORKLOADS[name]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    splits = fab.fa_fwd_ex_splits(w.B, w.H, w.N, w.Nkv, sms) if w.splits == 0 else w.splits
+    q, k, v = I.make(w)
+    check(w.dtype, q, k, v, splits)
+
+
+@pytest.mark.parametrize("name", ["gqa_b2h32kv8_n8192_d128", "causal_b2h32_n8192_d128",
+                                  "f16_b2h32_n8192_d128"])
+def test_headline_variants_sampled_rows(name):
+    from .gpu_util import edge_rows
+    w = I.WORKLOADS[name]
+    q, k, v = I.make(w)
+    o, lse = run_fa_ex(q, k, v, w.dtype, 1, causal=w.causal)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    err_o, err_l = compare_ex(w.dtype, o, lse, q, k, v, rows=edge_rows(w, w.oracle_rows), causal=w.causal)
+    assert err_o <= tol_o_dtype(w.dtype) and err_l <= TOL_LSE, (err_o, err_l)
