@@ -310,7 +310,7 @@ def run_ours(args, w):
     splits = w.splits
     if splits == 0:  # as many key partitions as fill one wave of SMs
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        splits = fab.fa_fwd_ex_splits(w.B, w.H, w.N, w.Nkv, sms)
+        splits = fab.fa_fwd_ex_splits(w.B, w.H, w.H_kv, w.N, w.Nkv, sms)
     wbytes = fab.fa_fwd_ex_workspace_size(w.B, w.H, w.N, w.Nkv, w.d, splits)
     work = torch.empty(max(wbytes, 16), dtype=torch.uint8, device=dev)  # caller-owned scratch
     kernels_per_step = 2 if wbytes else 1  # forward (+ merge of the partitions)

@@ -87,7 +87,7 @@ def load(path: str | None = None):
         lib.fa_fwd_ex_workspace_size.restype = sz
         lib.fa_fwd_ex_workspace_size.argtypes = [i64, i64, i64, i64, i64, c_int]
         lib.fa_fwd_ex_splits.restype = c_int
-        lib.fa_fwd_ex_splits.argtypes = [i64, i64, i64, i64, c_int]
+        lib.fa_fwd_ex_splits.argtypes = [i64, i64, i64, i64, i64, c_int]
         lib.fa_fwd_ex_static.restype = c_int
         lib.fa_fwd_ex_static.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, c_int,
                                          c_int, vp]
@@ -134,8 +134,8 @@ def fa_fwd_ex_workspace_size(B: int, H: int, N_q: int, N_kv: int, d: int, num_sp
     return int(load().fa_fwd_ex_workspace_size(B, H, N_q, N_kv, d, num_splits))
 
 
-def fa_fwd_ex_splits(B: int, H: int, N_q: int, N_kv: int, num_sms: int) -> int:
-    return int(load().fa_fwd_ex_splits(B, H, N_q, N_kv, num_sms))
+def fa_fwd_ex_splits(B: int, H: int, H_kv: int, N_q: int, N_kv: int, num_sms: int) -> int:
+    return int(load().fa_fwd_ex_splits(B, H, H_kv, N_q, N_kv, num_sms))
 
 
 def fa_fwd_ex_static(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, H_kv: int,

@@ -90,8 +90,10 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 // 3-D tiled map over [BH, N, d] (innermost first), 128-byte swizzle, boxes of
-// 128 bytes x 128 rows x 1 head; rows past N read as zero and are not written.
-int encode_map(CUtensorMap* map, const void* base, int dtype, int64_t BH, int64_t N, int64_t d) {
+// 128 bytes x box_rows rows x box_heads heads (128 x 1 normally; Nq x group
+// for packed grouped heads); rows past N read as zero and are not written.
+int encode_map(CUtensorMap* map, const void* base, int dtype, int64_t BH, int64_t N, int64_t d,
+               uint32_t box_rows = 128, uint32_t box_heads = 1) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (enc == nullptr) {
         set_error("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)",
@@ -103,7 +105,7 @@ int encode_map(CUtensorMap* map, const void* base, int dtype, int64_t BH, int64_
                                 static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elem,
                                    static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * elem};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem), 128, 1};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem), box_rows, box_heads};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUtensorMapDataType type = dtype == FA_DTYPE_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                      : dtype == FA_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
@@ -152,6 +154,21 @@ struct SplitPlan {
     int tiles_per_split;
     int n_kv_tiles;
 };
+
+// Grouped query heads whose Nq rows all fit one 128-row tile are packed: one
+// CTA per key/value head serves its `group` query heads (a decode step reads
+// each key/value tile once instead of once per query head).
+bool packed_heads(int64_t H, int64_t H_kv, int64_t N_q) {
+    const int64_t group = H / H_kv;
+    return group > 1 && N_q * group <= 128;
+}
+
+// CTAs of one key partition: query blocks of 256 rows per head (per key/value
+// head when packed).
+int64_t ctas_per_partition(int64_t B, int64_t H, int64_t H_kv, int64_t N_q) {
+    if (packed_heads(H, H_kv, N_q)) return B * H_kv;
+    return B * H * ((N_q + 255) / 256);
+}
 constexpr int kMaxSplits = 32;  // the merge kernel holds one partition per lane
 
 SplitPlan plan_splits(int64_t N_kv, int num_splits) {
@@ -196,8 +213,7 @@ int validate_ex(const void* q, const void* k, const void* v, const void* o, cons
     if (N_q * d * elem >= (int64_t(1) << 40) || N_kv * d * elem >= (int64_t(1) << 40))
         return FA_ERR_UNSUPPORTED;
     const SplitPlan sp = plan_splits(N_kv, num_splits);
-    const int64_t qblocks = (N_q + 255) / 256;
-    if (qblocks * sp.splits > kInt32Max / BH) return FA_ERR_UNSUPPORTED;  // one CTA per 256 rows per partition
+    if (ctas_per_partition(B, H, H_kv, N_q) > kInt32Max / sp.splits) return FA_ERR_UNSUPPORTED;  // grid size
     const uintptr_t mask = 15;
     if ((reinterpret_cast<uintptr_t>(q) & mask) || (reinterpret_cast<uintptr_t>(k) & mask) ||
         (reinterpret_cast<uintptr_t>(v) & mask) || (reinterpret_cast<uintptr_t>(o) & mask))
@@ -232,12 +248,15 @@ int launch_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     const bool causal = (dtype_arg & FA_FLAG_CAUSAL) != 0;
     const int64_t BH = B * H;
     const SplitPlan sp = plan_splits(N_kv, num_splits);
+    const bool pack = packed_heads(H, H_kv, N_q);
+    const uint32_t qbox_rows = pack ? static_cast<uint32_t>(N_q) : 128u;
+    const uint32_t qbox_heads = pack ? static_cast<uint32_t>(H / H_kv) : 1u;
     CUtensorMap mq, mk, mv, mo;
     int st;
-    if ((st = encode_map(&mq, q, dtype, BH, N_q, d)) != FA_OK) return st;
+    if ((st = encode_map(&mq, q, dtype, BH, N_q, d, qbox_rows, qbox_heads)) != FA_OK) return st;
     if ((st = encode_map(&mk, k, dtype, B * H_kv, N_kv, d)) != FA_OK) return st;
     if ((st = encode_map(&mv, v, dtype, B * H_kv, N_kv, d)) != FA_OK) return st;
-    if ((st = encode_map(&mo, o, dtype, BH, N_q, d)) != FA_OK) return st;
+    if ((st = encode_map(&mo, o, dtype, BH, N_q, d, qbox_rows, qbox_heads)) != FA_OK) return st;
 
     fa::FwdParams p{};
     p.status = device_status_words(&st);
@@ -246,7 +265,8 @@ int launch_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     p.Nq = static_cast<int>(N_q);
     p.Nkv = static_cast<int>(N_kv);
     p.n_kv_tiles = sp.n_kv_tiles;
-    p.n_q_blocks = static_cast<int>((N_q + 255) / 256);
+    p.pack = pack ? 1 : 0;
+    p.n_q_blocks = pack ? 1 : static_cast<int>((N_q + 255) / 256);
     p.H = static_cast<int>(H);
     p.H_kv = static_cast<int>(H_kv);
     p.group = static_cast<int>(H / H_kv);
@@ -263,7 +283,7 @@ int launch_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     } else {
         p.lse = lse;
     }
-    const unsigned int grid = static_cast<unsigned int>(BH * p.n_q_blocks * sp.splits);
+    const unsigned int grid = static_cast<unsigned int>(ctas_per_partition(B, H, H_kv, N_q) * sp.splits);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     cudaError_t e;
@@ -334,9 +354,9 @@ size_t fa_fwd_ex_workspace_size(int64_t B, int64_t H, int64_t N_q, int64_t N_kv,
     return workspace_bytes_for(B, H, N_q, d, plan_splits(N_kv, num_splits));
 }
 
-int fa_fwd_ex_splits(int64_t B, int64_t H, int64_t N_q, int64_t N_kv, int num_sms) {
-    if (B < 1 || H < 1 || N_q < 1 || N_kv < 1 || num_sms < 1) return 1;
-    const int64_t ctas = B * H * ((N_q + 255) / 256);
+int fa_fwd_ex_splits(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int num_sms) {
+    if (B < 1 || H < 1 || H_kv < 1 || H % H_kv != 0 || N_q < 1 || N_kv < 1 || num_sms < 1) return 1;
+    const int64_t ctas = ctas_per_partition(B, H, H_kv, N_q);
     if (ctas >= num_sms) return 1;
     const int64_t want = num_sms / ctas;  // fill about one wave
     return plan_splits(N_kv, static_cast<int>(want > kMaxSplits ? kMaxSplits : want)).splits;

@@ -262,27 +262,41 @@ __device__ __forceinline__ float sum8(const uint64_t (&a)[4]) {
 // and m, l, lq go to the partition's slab of the workspace.  Not inlined: it
 // runs once per CTA and keeps its address arithmetic out of the main loop.
 template <int D>
-__device__ __noinline__ void store_partial(const FwdParams& p, uint32_t tO, int row, float m_ref,
+__device__ __noinline__ void store_partial(const FwdParams& p, uint32_t tO, long long qrow, float m_ref,
                                            float l, float lq) {
+    // qrow: the query row's index in a partition's slab (B*H*Nq rows), or -1
+    // for a tile row that is not a query row
     const unsigned int split = blockIdx.x % static_cast<unsigned>(p.splits);
-    const unsigned int cta = blockIdx.x / static_cast<unsigned>(p.splits);
-    const size_t bh = cta / static_cast<unsigned>(p.n_q_blocks);
-    // rows of one partition's slab: B*H*Nq (the grid holds B*H*n_q_blocks*splits CTAs)
-    const size_t slab = static_cast<size_t>(gridDim.x / p.splits / p.n_q_blocks) * p.Nq;
-    const size_t r = split * slab + bh * p.Nq + row;
+    const size_t slab = static_cast<size_t>(gridDim.x / p.splits / p.n_q_blocks) * p.Nq *
+                        (p.pack ? static_cast<size_t>(p.group) : 1u);
+    const size_t r = split * slab + static_cast<size_t>(qrow);
 #pragma unroll
     for (int q = 0; q < D / 32; ++q) {
         uint32_t o[32];
         tmem_ld32(tO + 32u * q, o);
         tmem_ld_wait(o);
-        if (row < p.Nq) {
+        if (qrow >= 0) {
             uint4* dst = reinterpret_cast<uint4*>(p.o_part + r * D + q * 32);
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
                 dst[ch] = make_uint4(o[4 * ch], o[4 * ch + 1], o[4 * ch + 2], o[4 * ch + 3]);
         }
     }
-    if (row < p.Nq) *reinterpret_cast<float4*>(p.ml_part + r * 4) = make_float4(m_ref, l, lq, 0.0f);
+    if (qrow >= 0) *reinterpret_cast<float4*>(p.ml_part + r * 4) = make_float4(m_ref, l, lq, 0.0f);
+}
+
+// Zero the rows of the two query tiles that a packed launch does not load
+// (row >= `rows` of tile 0, all of tile 1), one warp, before the Q load.
+template <int kTileBytes, int kAtoms, int kAtomBytes>
+__device__ __forceinline__ void zero_unloaded_q(uint8_t* q_tiles, int rows, int lane) {
+    for (int a = 0; a < kAtoms; ++a) {
+        uint4* t0 = reinterpret_cast<uint4*>(q_tiles + a * kAtomBytes);
+        for (int i = rows * 8 + lane; i < 128 * 8; i += 32) t0[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    uint4* t1 = reinterpret_cast<uint4*>(q_tiles + kTileBytes);
+    for (int i = lane; i < kTileBytes / 16; i += 32) t1[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    __syncwarp();
 }
 
 // Round `n16` 16-byte groups of fp32 in shared memory to TF32 in place
@@ -341,12 +355,20 @@ __device__ void produce_tf32(const CUtensorMap& map_q, const CUtensorMap& map_k,
     int nk = 0, nv = 0;  // K and V tiles whose loads were issued
     bool q_issued = false;
     bool ok = true;
+    if (p.pack) zero_unloaded_q<C::kTileBytes, C::kAtoms, C::kAtomBytes>(smem + C::kOffQ, p.Nq * p.group, lane);
     if (lane == 0) {
-        mbar_arrive_expect_tx(bar(C::kBarQRaw), 2u * C::kTileBytes);
-        for (int w = 0; w < 2; ++w)
+        if (p.pack) {
+            mbar_arrive_expect_tx(bar(C::kBarQRaw), static_cast<uint32_t>(C::kAtoms * p.Nq * p.group * 128));
             for (int a = 0; a < C::kAtoms; ++a)
-                tma_load_3d(sbase + C::kOffQ + w * C::kTileBytes + a * C::kAtomBytes, &map_q,
-                            bar(C::kBarQRaw), a * C::kAtomElems, row0 + w * kTileM, bh, once);
+                tma_load_3d(sbase + C::kOffQ + a * C::kAtomBytes, &map_q, bar(C::kBarQRaw),
+                            a * C::kAtomElems, 0, bh * p.group, once);
+        } else {
+            mbar_arrive_expect_tx(bar(C::kBarQRaw), 2u * C::kTileBytes);
+            for (int w = 0; w < 2; ++w)
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_3d(sbase + C::kOffQ + w * C::kTileBytes + a * C::kAtomBytes, &map_q,
+                                bar(C::kBarQRaw), a * C::kAtomElems, row0 + w * kTileM, bh, once);
+        }
     }
     q_issued = true;
     ok = all_ok(wait_phase(bar(C::kBarQRaw), 0, abort_flag, p, 20));
@@ -421,14 +443,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh = static_cast<int>(cta / static_cast<unsigned>(p.n_q_blocks));
     // key/value head of this query head (grouped-query attention: H / H_kv
     // query heads share one key/value head)
-    const int kvh = (bh / p.H) * p.H_kv + (bh % p.H) / p.group;
+    // packed: bh is the key/value head itself; otherwise its query head's
+    const int kvh = p.pack ? bh : (bh / p.H) * p.H_kv + (bh % p.H) / p.group;
+    // rows of query tile 0 that hold query rows in a packed launch
+    const int pack_rows = p.pack ? p.Nq * p.group : 0;
     const int row0 = qb * 2 * kTileM;
     // key tiles this query block can see: all, or under the causal mask
     // those up to the last key its last row sees
     int n_tiles_block = p.n_kv_tiles;
     if (kCausal) {
-        const long long lim = min(static_cast<long long>(p.Nkv),
-                                  static_cast<long long>(row0) + 2 * kTileM + p.causal_offset);
+        // last query index of the block (packed: every row has i < Nq)
+        const long long last_i = p.pack ? p.Nq - 1 : static_cast<long long>(row0) + 2 * kTileM - 1;
+        const long long lim = min(static_cast<long long>(p.Nkv), last_i + 1 + p.causal_offset);
         n_tiles_block = lim <= 0 ? 0 : static_cast<int>((lim + kTileN - 1) / kTileN);
     }
     const int t_begin = static_cast<int>(split) * p.tiles_per_split;
@@ -492,16 +518,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         // no visible key: nothing to load or multiply
       } else if (warp == kLoadWarp) {
         // ------------------------------------------------------ TMA producer
+        if (!TF32 && p.pack) zero_unloaded_q<C::kTileBytes, C::kAtoms, C::kAtomBytes>(smem + C::kOffQ, pack_rows, lane);
         if constexpr (TF32) {
             produce_tf32<D>(map_q, map_k, map_v, p, smem, sbase, lane, row0, bh, kvh, t_begin, T, abort_flag);
         } else if (lane == 0) {
             const uint64_t keep = policy_evict_last();   // K/V: read by every query block of the head
             const uint64_t once = policy_evict_first();  // Q: read once
-            mbar_arrive_expect_tx(bar(C::kBarQFull), 2u * C::kTileBytes);
-            for (int w = 0; w < 2; ++w)
+            if (p.pack) {
+                // Nq rows x group heads into the first rows of tile 0
+                mbar_arrive_expect_tx(bar(C::kBarQFull), static_cast<uint32_t>(C::kAtoms * pack_rows * 128));
                 for (int a = 0; a < C::kAtoms; ++a)
-                    tma_load_3d(sbase + C::kOffQ + w * C::kTileBytes + a * C::kAtomBytes, &map_q,
-                                bar(C::kBarQFull), a * C::kAtomElems, row0 + w * kTileM, bh, once);
+                    tma_load_3d(sbase + C::kOffQ + a * C::kAtomBytes, &map_q, bar(C::kBarQFull),
+                                a * C::kAtomElems, 0, bh * p.group, once);
+            } else {
+                mbar_arrive_expect_tx(bar(C::kBarQFull), 2u * C::kTileBytes);
+                for (int w = 0; w < 2; ++w)
+                    for (int a = 0; a < C::kAtoms; ++a)
+                        tma_load_3d(sbase + C::kOffQ + w * C::kTileBytes + a * C::kAtomBytes, &map_q,
+                                    bar(C::kBarQFull), a * C::kAtomElems, row0 + w * kTileM, bh, once);
+            }
             int nk = 0, nv = 0;  // K and V tiles whose loads were issued
             for (int j = 0; j < T; ++j) {
                 const int ks = j % C::kKStages;
@@ -630,9 +665,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // keys of this row's head visible to this row: all Nkv, or under the
         // causal mask those up to i + causal_offset (may be none)
+        // this thread's query row: (query head, query index i) and its row in
+        // the [B*H, Nq] outputs (-1: a tile row that holds no query row)
+        long long qi = row0 + w * kTileM + t;
+        long long out_row = qi < p.Nq ? static_cast<long long>(bh) * p.Nq + qi : -1;
+        if (p.pack) {
+            const int r = w * kTileM + t;
+            qi = r < pack_rows ? r % p.Nq : 0;
+            out_row = r < pack_rows ? (static_cast<long long>(bh) * p.group + r / p.Nq) * p.Nq + qi : -1;
+        }
         int row_limit = p.Nkv;
         if (kCausal) {
-            const long long lim = static_cast<long long>(row0 + w * kTileM + t) + p.causal_offset + 1;
+            const long long lim = qi + p.causal_offset + 1;
             row_limit = static_cast<int>(max(-1ll, min(static_cast<long long>(p.Nkv), lim)));
         }
         float m_ref = -INFINITY;  // reference maximum, base-2 scaled units
@@ -747,17 +791,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool got = wait_phase(bar(C::kBarOFull + w), 0, abort_flag, p, 11);
             ok = __all_sync(0xffffffffu, got);
         }
-        const int row = row0 + w * kTileM + t;
         uint8_t* stage = smem + C::kOffQ + w * C::kTileBytes;  // Q_w is free after its last S MMA
         const bool split_mode = p.splits > 1;
         if (ok && split_mode) {
             tc_fence_after();
             if (has_work) {
-                store_partial<D>(p, tO, row, m_ref, l, lq);
-            } else if (row < p.Nq) {
+                store_partial<D>(p, tO, out_row, m_ref, l, lq);
+            } else if (out_row >= 0) {
                 // an empty partition: weight 0 in the merge (its O slot is not read)
-                const size_t slab = static_cast<size_t>(gridDim.x / p.splits / p.n_q_blocks) * p.Nq;
-                const size_t r = split * slab + static_cast<size_t>(bh) * p.Nq + row;
+                const size_t slab = static_cast<size_t>(gridDim.x / p.splits / p.n_q_blocks) * p.Nq *
+                                    (p.pack ? static_cast<size_t>(p.group) : 1u);
+                const size_t r = split * slab + static_cast<size_t>(out_row);
                 *reinterpret_cast<float4*>(p.ml_part + r * 4) = make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
             }
         }
@@ -801,9 +845,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (p.lse != nullptr && row < p.Nq) {
+            if (p.lse != nullptr && out_row >= 0) {
                 const float lse2 = (l > 0.0f) ? (m_ref + log2f(l)) : -INFINITY;
-                p.lse[static_cast<size_t>(bh) * static_cast<size_t>(p.Nq) + row] = lse2 * 0.69314718055994531f;
+                p.lse[out_row] = lse2 * 0.69314718055994531f;
             }
             fence_proxy_async_smem();
         }
@@ -812,12 +856,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t == 0) {
             const bool all_in = wait_phase(bar(C::kBarEpi + w), 0, abort_flag, p, 12);
             // a tile lying entirely past Nq has nothing to store
-            if (all_in && !split_mode && !*abort_flag && row0 + w * kTileM < p.Nq) {
-                for (int a = 0; a < C::kAtoms; ++a)
-                    tma_store_3d(&map_o, smem_u32(stage + a * C::kAtomBytes), a * C::kAtomElems,
-                                 row0 + w * kTileM, bh);
-                tma_store_commit();
-                tma_store_wait_read();
+            if (all_in && !split_mode && !*abort_flag) {
+                if (p.pack) {
+                    // the Nq x group query rows of tile 0 (tile 1 holds none)
+                    if (w == 0) {
+                        for (int a = 0; a < C::kAtoms; ++a)
+                            tma_store_3d(&map_o, smem_u32(stage + a * C::kAtomBytes), a * C::kAtomElems, 0,
+                                         bh * p.group);
+                        tma_store_commit();
+                        tma_store_wait_read();
+                    }
+                } else if (row0 + w * kTileM < p.Nq) {
+                    for (int a = 0; a < C::kAtoms; ++a)
+                        tma_store_3d(&map_o, smem_u32(stage + a * C::kAtomBytes), a * C::kAtomElems,
+                                     row0 + w * kTileM, bh);
+                    tma_store_commit();
+                    tma_store_wait_read();
+                }
             }
         }
     }

@@ -15,6 +15,12 @@ struct DevStatus {
 };
 
 // Parameters of one forward launch, passed by value.
+//
+// Packed launches (pack = 1; grouped heads with Nq * group <= 128, e.g. a
+// decode step): a CTA serves one key/value head, and query tile 0 holds the
+// Nq rows of each of its `group` query heads, row r = g * Nq + i for query
+// head (key/value head * group + g) and query index i.  The Q and O tensor
+// maps then use boxes of Nq rows x group heads.
 struct FwdParams {
     float* lse;              // fp32 [B*H, Nq] or nullptr (unsplit launches)
     DevStatus* status;       // device status word of the current device
@@ -26,6 +32,7 @@ struct FwdParams {
     int H;                   // query heads
     int group;               // query heads per key/value head (H / H_kv)
     int H_kv;                // key / value heads
+    int pack;                // 1: grouped heads packed into one tile (see below)
     int causal;              // 1: query i sees keys j <= i + causal_offset only
     int causal_offset;       // Nkv - Nq (the last query sees every key)
     int splits;              // key-range partitions per query block (1 = none)

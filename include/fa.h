@@ -138,11 +138,15 @@ size_t fa_fwd_ex_workspace_size(int64_t B, int64_t H, int64_t N_q, int64_t N_kv,
                                 int64_t d, int num_splits);
 
 /*
- * A partition count that fills about one wave of `num_sms` SMs: 1 when
- * B * H * ceil(N_q / 256) CTAs already fill the GPU, else
- * num_sms / that count (capped as above).  Pure host computation.
+ * A partition count that fills about one wave of `num_sms` SMs: 1 when the
+ * CTAs of one partition already fill the GPU, else num_sms / that count
+ * (capped as above).  A partition has B * H * ceil(N_q / 256) CTAs, or
+ * B * H_kv when the grouped query heads are packed (H_kv < H and
+ * N_q * H / H_kv <= 128: one CTA serves all query heads of a key/value head,
+ * e.g. for decode steps).  Pure host computation; 1 for invalid sizes.
  */
-int fa_fwd_ex_splits(int64_t B, int64_t H, int64_t N_q, int64_t N_kv, int num_sms);
+int fa_fwd_ex_splits(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv,
+                     int num_sms);
 
 /*
  * fa_fwd_ex_static — fa_fwd_ex for callers that cannot allocate device

@@ -129,9 +129,13 @@ def test_split_planning(lib):
     assert fab.fa_fwd_ex_workspace_size(1, 1, 10, 1 << 20, 64, 64) == 32 * 10 * 68 * 4
     # no empty partition: 5 tiles in 4 requested -> 3 partitions of 2, 2, 1 tiles
     assert fab.fa_fwd_ex_workspace_size(1, 1, 1, 5 * 128, 64, 4) == 3 * 1 * 68 * 4
-    assert fab.fa_fwd_ex_splits(1, 1, 512, 512, 152) == 4          # 2 CTAs; capped at 4 key tiles
-    assert fab.fa_fwd_ex_splits(2, 32, 8192, 8192, 152) == 1       # 2048 CTAs fill the GPU
-    assert fab.fa_fwd_ex_splits(2, 4, 1000, 1000, 152) == 4
+    assert fab.fa_fwd_ex_splits(1, 1, 1, 512, 512, 152) == 4        # 2 CTAs; capped at 4 key tiles
+    assert fab.fa_fwd_ex_splits(2, 32, 32, 8192, 8192, 152) == 1    # 2048 CTAs fill the GPU
+    assert fab.fa_fwd_ex_splits(2, 4, 4, 1000, 1000, 152) == 4
+    # packed grouped heads: one CTA per key/value head
+    assert fab.fa_fwd_ex_splits(8, 32, 8, 1, 16384, 152) == 2       # 64 CTAs
+    assert fab.fa_fwd_ex_splits(8, 32, 32, 1, 16384, 152) == 1      # no grouping: 256 CTAs
+    assert fab.fa_fwd_ex_splits(1, 8, 2, 64, 4096, 152) == 16       # 64 x 4 rows > 128: 8 CTAs; 19 wanted, 2 of 32 tiles each
 
 
 def test_dtype_flags(lib):

@@ -105,7 +105,7 @@ def test_workloads_in_bench_launch_configuration(name):
     them: fa_fwd_ex with the key partitions that fill one wave of SMs."""
     w = I.WORKLOADS[name]
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    splits = fab.fa_fwd_ex_splits(w.B, w.H, w.N, w.Nkv, sms) if w.splits == 0 else w.splits
+    splits = fab.fa_fwd_ex_splits(w.B, w.H, w.H_kv, w.N, w.Nkv, sms) if w.splits == 0 else w.splits
     q, k, v = I.make(w)
     check(w.dtype, q, k, v, splits)
 
@@ -120,3 +120,26 @@ def test_headline_variants_sampled_rows(name):
     assert np.isfinite(o).all() and np.isfinite(lse).all()
     err_o, err_l = compare_ex(w.dtype, o, lse, q, k, v, rows=edge_rows(w, w.oracle_rows), causal=w.causal)
     assert err_o <= tol_o_dtype(w.dtype) and err_l <= TOL_LSE, (err_o, err_l)
+
+
+@pytest.mark.parametrize("Nq,G", [(1, 2), (1, 8), (16, 4), (32, 4), (3, 5)])
+@pytest.mark.parametrize("splits", [1, 4])
+def test_packed_grouped_heads(Nq, G, splits):
+    """Query heads of one key/value head packed into one tile (Nq * G <= 128),
+    including exactly 128 packed rows and a group size that is not a power
+    of two."""
+    H_kv = 3
+    q, k, v = I.make_general(2, H_kv * G, H_kv, Nq, 1500, 128, "bf16", seed=500 + Nq * G + splits)
+    check("bf16", q, k, v, splits)
+
+
+def test_packed_causal_and_fp32():
+    from .gpu_util import compare_ex, run_fa_ex
+    q, k, v = I.make_general(1, 8, 2, 16, 700, 64, "bf16", seed=520)
+    o, lse = run_fa_ex(q, k, v, "bf16", 3, causal=True)
+    err_o, err_l = compare_ex("bf16", o, lse, q, k, v, causal=True)
+    assert err_o <= tol_o_dtype("bf16") and err_l <= TOL_LSE
+    q, k, v = I.make_general(1, 8, 2, 4, 900, 64, "f32", seed=521)
+    check("f32", q, k, v, 2)
+    q, k, v = I.make_general(2, 16, 4, 1, 3000, 64, "f16", seed=522)
+    check("f16", q, k, v, 4)
