@@ -92,11 +92,14 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources: ties a stored ncu traffic figure to the
+    """Hash of the forward path's CUDA sources (every file of csrc/ except
+    the backward pass's fa_bwd*): ties a stored ncu traffic figure to the
     kernel it was measured on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_tiled_attention_04_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
+        if name.startswith("fa_bwd"):
+            continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
