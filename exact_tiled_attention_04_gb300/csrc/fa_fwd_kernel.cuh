@@ -422,7 +422,9 @@ __device__ void produce_tf32(const CUtensorMap& map_q, const CUtensorMap& map_k,
     }
 }
 
-template <bool TF32, int D, bool F16 = false, bool kCausal = false>
+// kOneTile: a packed launch (p.pack = 1), where query tile 1 holds no row;
+// a template parameter so that unpacked launches carry none of its checks.
+template <bool TF32, int D, bool F16 = false, bool kCausal = false, bool kOneTile = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
@@ -437,6 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = static_cast<int>(threadIdx.x) / 32;
     const int lane = static_cast<int>(threadIdx.x) % 32;
     // blockIdx.x = ((bh * n_q_blocks) + qb) * splits + split
+    // grouped heads packed into query tile 0 (p.pack; always set when kOneTile)
+    const bool pack = kOneTile || p.pack != 0;
     const unsigned int split = blockIdx.x % static_cast<unsigned>(p.splits);
     const unsigned int cta = blockIdx.x / static_cast<unsigned>(p.splits);
     const int qb = static_cast<int>(cta % static_cast<unsigned>(p.n_q_blocks));
@@ -444,16 +448,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // key/value head of this query head (grouped-query attention: H / H_kv
     // query heads share one key/value head)
     // packed: bh is the key/value head itself; otherwise its query head's
-    const int kvh = p.pack ? bh : (bh / p.H) * p.H_kv + (bh % p.H) / p.group;
+    const int kvh = pack ? bh : (bh / p.H) * p.H_kv + (bh % p.H) / p.group;
     // rows of query tile 0 that hold query rows in a packed launch
-    const int pack_rows = p.pack ? p.Nq * p.group : 0;
+    const int pack_rows = pack ? p.Nq * p.group : 0;
+    // packed launches hold no query row in tile 1: its issuer and softmax
+    // warpgroup sit out, and K/V stages are released by tile 0 alone
+    constexpr bool one_tile = kOneTile;
     const int row0 = qb * 2 * kTileM;
     // key tiles this query block can see: all, or under the causal mask
     // those up to the last key its last row sees
     int n_tiles_block = p.n_kv_tiles;
     if (kCausal) {
         // last query index of the block (packed: every row has i < Nq)
-        const long long last_i = p.pack ? p.Nq - 1 : static_cast<long long>(row0) + 2 * kTileM - 1;
+        const long long last_i = pack ? p.Nq - 1 : static_cast<long long>(row0) + 2 * kTileM - 1;
         const long long lim = min(static_cast<long long>(p.Nkv), last_i + 1 + p.causal_offset);
         n_tiles_block = lim <= 0 ? 0 : static_cast<int>((lim + kTileN - 1) / kTileN);
     }
@@ -469,13 +476,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- setup
     if (threadIdx.x == 0) {
         mbar_init(bar(C::kBarQFull), 1);
+        const uint32_t issuers = one_tile ? 1u : 2u;
         for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(bar(C::kBarKFull + s), 1);
-            mbar_init(bar(C::kBarKEmpty + s), 2);  // both issuers' commits
+            mbar_init(bar(C::kBarKEmpty + s), issuers);  // every active issuer's commit
         }
         for (int s = 0; s < C::kVStages; ++s) {
             mbar_init(bar(C::kBarVFull + s), 1);
-            mbar_init(bar(C::kBarVEmpty + s), 2);
+            mbar_init(bar(C::kBarVEmpty + s), issuers);
         }
         for (int w = 0; w < 2; ++w) {
             mbar_init(bar(C::kBarSFull + w), 1);
@@ -518,13 +526,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // no visible key: nothing to load or multiply
       } else if (warp == kLoadWarp) {
         // ------------------------------------------------------ TMA producer
-        if (!TF32 && p.pack) zero_unloaded_q<C::kTileBytes, C::kAtoms, C::kAtomBytes>(smem + C::kOffQ, pack_rows, lane);
+        if (!TF32 && pack) zero_unloaded_q<C::kTileBytes, C::kAtoms, C::kAtomBytes>(smem + C::kOffQ, pack_rows, lane);
         if constexpr (TF32) {
             produce_tf32<D>(map_q, map_k, map_v, p, smem, sbase, lane, row0, bh, kvh, t_begin, T, abort_flag);
         } else if (lane == 0) {
             const uint64_t keep = policy_evict_last();   // K/V: read by every query block of the head
             const uint64_t once = policy_evict_first();  // Q: read once
-            if (p.pack) {
+            if (pack) {
                 // Nq rows x group heads into the first rows of tile 0
                 mbar_arrive_expect_tx(bar(C::kBarQFull), static_cast<uint32_t>(C::kAtoms * pack_rows * 128));
                 for (int a = 0; a < C::kAtoms; ++a)
@@ -578,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // never behind the other tile's instructions.  Both read the same K/V
         // stages; each stage is released when both issuers' products that
         // read it have completed (empty barriers count two commits).
-        if (lane == 0) {
+        if (lane == 0 && !(one_tile && warp == kMmaWarp2)) {
             const int w = (warp == kMmaWarp) ? 0 : 1;
             const uint32_t dS = tmem + 128u * static_cast<uint32_t>(w);
             const uint32_t dO = tmem + 256u + static_cast<uint32_t>(D * w);
@@ -662,6 +670,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tS = tmem + lane_off + 128u * static_cast<uint32_t>(w);
         const uint32_t tO = tmem + lane_off + 256u + static_cast<uint32_t>(D * w);
         const float c = p.scale_log2;
+        const bool active = !(one_tile && w == 1);  // this warpgroup's tile has rows
+        const bool take_turns = !one_tile;
 
         // keys of this row's head visible to this row: all Nkv, or under the
         // causal mask those up to i + causal_offset (may be none)
@@ -669,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the [B*H, Nq] outputs (-1: a tile row that holds no query row)
         long long qi = row0 + w * kTileM + t;
         long long out_row = qi < p.Nq ? static_cast<long long>(bh) * p.Nq + qi : -1;
-        if (p.pack) {
+        if (pack) {
             const int r = w * kTileM + t;
             qi = r < pack_rows ? r % p.Nq : 0;
             out_row = r < pack_rows ? (static_cast<long long>(bh) * p.group + r / p.Nq) * p.Nq + qi : -1;
@@ -688,14 +698,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The two softmax warpgroups take turns (0, 1, 0, 1, ...): one runs its
         // exponentials while the other tile's products occupy the tensor core
         // (see kTurnAfterHalf for how far the turns overlap).
-        if (w == 1 && lane == 0) mbar_arrive(bar(C::kBarTurn + 0));
-        for (int j = 0; j < T; ++j) {  // T <= 0: no key tile
+        if (take_turns && w == 1 && lane == 0) mbar_arrive(bar(C::kBarTurn + 0));
+        const int T_rows = active ? T : 0;
+        for (int j = 0; j < T_rows; ++j) {  // T <= 0: no key tile
             bool got = wait_phase(bar(C::kBarSFull + w), j & 1, abort_flag, p, 10);
             ok = __all_sync(0xffffffffu, got);
             if (!ok) break;
-            got = wait_phase(bar(C::kBarTurn + w), j & 1, abort_flag, p, 13);
-            ok = __all_sync(0xffffffffu, got);
-            if (!ok) break;
+            if (take_turns) {
+                got = wait_phase(bar(C::kBarTurn + w), j & 1, abort_flag, p, 13);
+                ok = __all_sync(0xffffffffu, got);
+                if (!ok) break;
+            }
             tc_fence_after();
 
             uint32_t s[4][32];
@@ -772,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::kBarPFull + 2 * w + h));
-                if (h == C::kTurnAfterHalf && lane == 0) mbar_arrive(bar(C::kBarTurn + (1 - w)));
+                if (take_turns && h == C::kTurnAfterHalf && lane == 0) mbar_arrive(bar(C::kBarTurn + (1 - w)));
             }
             // l: fp32 sum of the weights (gives lse).  lq: the same sum with
             // the tile's largest weight replaced by its value as rounded for
@@ -787,25 +800,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // ------------------------------------------------------- epilogue
-        if (ok && has_work) {
+        if (ok && has_work && active) {
             bool got = wait_phase(bar(C::kBarOFull + w), 0, abort_flag, p, 11);
             ok = __all_sync(0xffffffffu, got);
         }
         uint8_t* stage = smem + C::kOffQ + w * C::kTileBytes;  // Q_w is free after its last S MMA
         const bool split_mode = p.splits > 1;
-        if (ok && split_mode) {
+        if (ok && split_mode && active) {
             tc_fence_after();
             if (has_work) {
                 store_partial<D>(p, tO, out_row, m_ref, l, lq);
             } else if (out_row >= 0) {
                 // an empty partition: weight 0 in the merge (its O slot is not read)
                 const size_t slab = static_cast<size_t>(gridDim.x / p.splits / p.n_q_blocks) * p.Nq *
-                                    (p.pack ? static_cast<size_t>(p.group) : 1u);
+                                    (pack ? static_cast<size_t>(p.group) : 1u);
                 const size_t r = split * slab + static_cast<size_t>(out_row);
                 *reinterpret_cast<float4*>(p.ml_part + r * 4) = make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
             }
         }
-        if (ok && !split_mode) {
+        if (ok && !split_mode && active) {
             tc_fence_after();
             const float inv_l = lq > 0.0f ? 1.0f / lq : 0.0f;
 #pragma unroll
@@ -857,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool all_in = wait_phase(bar(C::kBarEpi + w), 0, abort_flag, p, 12);
             // a tile lying entirely past Nq has nothing to store
             if (all_in && !split_mode && !*abort_flag) {
-                if (p.pack) {
+                if (pack) {
                     // the Nq x group query rows of tile 0 (tile 1 holds none)
                     if (w == 0) {
                         for (int a = 0; a < C::kAtoms; ++a)
@@ -886,12 +899,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool TF32, int D, bool F16, bool kCausal>
+template <bool TF32, int D, bool F16, bool kCausal, bool kOneTile>
 cudaError_t launch_fwd_variant(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                const CUtensorMap& o, const FwdParams& p, unsigned int grid,
                                cudaStream_t stream) {
     using C = FwdCfg<TF32, D, F16>;
-    auto kern = fa_fwd_kernel<TF32, D, F16, kCausal>;
+    auto kern = fa_fwd_kernel<TF32, D, F16, kCausal, kOneTile>;
     // The register split above relies on the compiled kernel holding exactly
     // kLaunchRegs per thread; refuse to launch otherwise (a setmaxnreg.inc
     // without the registers behind it would never return).
@@ -909,13 +922,17 @@ cudaError_t launch_fwd_variant(const CUtensorMap& q, const CUtensorMap& k, const
 }  // namespace fa
 
 namespace fa {
-// Causal and unmasked kernels are separate instantiations: the unmasked one
-// keeps a tile's key count uniform across rows.
+// Causal and unmasked kernels are separate instantiations (the unmasked one
+// keeps a tile's key count uniform across rows), and so are packed and
+// unpacked ones.
 template <bool TF32, int D, bool F16 = false>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& o, const FwdParams& p, unsigned int grid,
                        cudaStream_t stream) {
-    return p.causal ? launch_fwd_variant<TF32, D, F16, true>(q, k, v, o, p, grid, stream)
-                    : launch_fwd_variant<TF32, D, F16, false>(q, k, v, o, p, grid, stream);
+    if (p.pack)
+        return p.causal ? launch_fwd_variant<TF32, D, F16, true, true>(q, k, v, o, p, grid, stream)
+                        : launch_fwd_variant<TF32, D, F16, false, true>(q, k, v, o, p, grid, stream);
+    return p.causal ? launch_fwd_variant<TF32, D, F16, true, false>(q, k, v, o, p, grid, stream)
+                    : launch_fwd_variant<TF32, D, F16, false, false>(q, k, v, o, p, grid, stream);
 }
 }  // namespace fa
