@@ -6,8 +6,9 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 that package: the two share no code.
 
 The arithmetic lives in ``attn_oracle.c`` (plain three-pass softmax attention
-in fp64, one query row at a time); this module only compiles it with gcc and
-marshals numpy arrays through ctypes.
+in fp64, one query row at a time) and ``attn_bwd_oracle.c`` (its exact
+gradients, row by row); this module only compiles them with gcc and marshals
+numpy arrays through ctypes.
 
     O = softmax(scale * Q K^T) V,   lse_i = log sum_j exp(scale * q_i . k_j)
 
@@ -26,6 +27,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "attn_bwd_oracle.c")]
 _LIB_NAME = "liboracle_attn.so"
 _lock = threading.Lock()
 _lib = None
@@ -41,11 +43,11 @@ def build(out_dir: str | None = None, mutant: int = 0, force: bool = False) -> s
     name = _LIB_NAME if mutant == 0 else f"liboracle_attn_mutant{mutant}.so"
     path = os.path.join(out_dir, name)
     if (not force and os.path.exists(path)
-            and os.path.getmtime(path) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(path) >= os.path.getmtime(src) for src in _SRCS)):
         return path
     tmp = f"{path}.{os.getpid()}.tmp"
     cmd = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-pthread",
-           f"-DORACLE_MUTANT={int(mutant)}", _SRC, "-o", tmp, "-lm"]
+           f"-DORACLE_MUTANT={int(mutant)}", *_SRCS, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, path)
     return path
@@ -67,6 +69,15 @@ def _bind(path: str):
         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
         ctypes.c_int64, ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    shape = [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 6 + [ctypes.c_double, ctypes.c_int]
+    lib.oracle_attention_bwd_f64.restype = ctypes.c_int
+    lib.oracle_attention_bwd_f64.argtypes = shape + [ctypes.c_void_p] * 3 + [ctypes.c_int]
+    lib.oracle_attention_bwd_dq_rows_f64.restype = ctypes.c_int
+    lib.oracle_attention_bwd_dq_rows_f64.argtypes = shape + [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]
+    lib.oracle_attention_bwd_dkv_cols_f64.restype = ctypes.c_int
+    lib.oracle_attention_bwd_dkv_cols_f64.argtypes = shape + [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
     return lib
 
 
@@ -161,3 +172,73 @@ def flops(B: int, H: int, N: int, d: int, rows: int | None = None) -> float:
     (2*N*d for the scores, 2*N*d for the weighted sum of V)."""
     r = B * H * N if rows is None else rows
     return 4.0 * r * N * d
+
+
+def _bwd_operands(q, k, v, dout):
+    q, k, v, dout = (np.ascontiguousarray(x, dtype=np.float32) for x in (q, k, v, dout))
+    if q.ndim != 4 or k.ndim != 4 or k.shape != v.shape or dout.shape != q.shape \
+            or q.shape[0] != k.shape[0] or q.shape[3] != k.shape[3] or q.shape[1] % k.shape[1]:
+        raise ValueError(f"incompatible shapes: q {q.shape}, k {k.shape}, v {v.shape}, "
+                         f"dout {dout.shape}")
+    B, H, Nq, d = (int(x) for x in q.shape)
+    H_kv, Nkv = int(k.shape[1]), int(k.shape[2])
+    return (q, k, v, dout), (B, H, H_kv, Nq, Nkv, d)
+
+
+def attention_bwd_f64(q, k, v, dout, scale: float, causal: bool = False, threads: int = 0,
+                      lib=None):
+    """Exact gradients of O = softmax(scale * Q K^T) V for the upstream
+    gradient dout, in fp64.  q, dout: [B, H, Nq, d]; k, v: [B, H_kv, Nkv, d]
+    (H_kv divides H).  Returns (dq, dk, dv) with the shapes of q, k, v.  The
+    softmax weights are recomputed from their definition (no saved lse)."""
+    lib = lib or load()
+    ops, dims = _bwd_operands(q, k, v, dout)
+    q, k, v, dout = ops
+    dq = np.empty(q.shape, dtype=np.float64)
+    dk = np.empty(k.shape, dtype=np.float64)
+    dv = np.empty(v.shape, dtype=np.float64)
+    rc = lib.oracle_attention_bwd_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data,
+                                      *dims, float(scale), int(bool(causal)), dq.ctypes.data,
+                                      dk.ctypes.data, dv.ctypes.data, int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_bwd_f64 failed with status {rc}")
+    return dq, dk, dv
+
+
+def attention_bwd_dq_rows_f64(q, k, v, dout, scale: float, rows, causal: bool = False,
+                              threads: int = 0, lib=None):
+    """dQ of the query rows (b, h, i) in `rows` ([R, 3]); returns fp64 [R, d].
+    Each row needs only its own scores, so this is cheap at any size."""
+    lib = lib or load()
+    ops, dims = _bwd_operands(q, k, v, dout)
+    q, k, v, dout = ops
+    rows_arr = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1, 3)
+    dq = np.empty((rows_arr.shape[0], dims[5]), dtype=np.float64)
+    rc = lib.oracle_attention_bwd_dq_rows_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                              dout.ctypes.data, *dims, float(scale),
+                                              int(bool(causal)), rows_arr.ctypes.data,
+                                              rows_arr.shape[0], dq.ctypes.data, int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_bwd_dq_rows_f64 failed with status {rc}")
+    return dq
+
+
+def attention_bwd_dkv_cols_f64(q, k, v, dout, scale: float, cols, causal: bool = False,
+                               threads: int = 0, lib=None):
+    """dK and dV of the keys (b, kv_head, j) in `cols` ([C, 3]); returns two
+    fp64 [C, d] arrays.  Every query row of each requested key/value head is
+    evaluated once (cost ~ 4 * group * Nq * Nkv * d per head)."""
+    lib = lib or load()
+    ops, dims = _bwd_operands(q, k, v, dout)
+    q, k, v, dout = ops
+    cols_arr = np.ascontiguousarray(cols, dtype=np.int64).reshape(-1, 3)
+    dk = np.empty((cols_arr.shape[0], dims[5]), dtype=np.float64)
+    dv = np.empty((cols_arr.shape[0], dims[5]), dtype=np.float64)
+    rc = lib.oracle_attention_bwd_dkv_cols_f64(q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                               dout.ctypes.data, *dims, float(scale),
+                                               int(bool(causal)), cols_arr.ctypes.data,
+                                               cols_arr.shape[0], dk.ctypes.data, dv.ctypes.data,
+                                               int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_bwd_dkv_cols_f64 failed with status {rc}")
+    return dk, dv
