@@ -93,6 +93,13 @@ def load(path: str | None = None):
                                          c_int, vp]
         lib.fa_fwd_ex_static_capacity.restype = sz
         lib.fa_fwd_ex_static_capacity.argtypes = []
+        bwd_args = [vp] * 9 + [i64] * 6 + [f32, c_int, vp, sz]
+        lib.fa_bwd.restype = c_int
+        lib.fa_bwd.argtypes = bwd_args + [vp]
+        lib.fa_bwd_validate.restype = c_int
+        lib.fa_bwd_validate.argtypes = bwd_args
+        lib.fa_bwd_workspace_size.restype = sz
+        lib.fa_bwd_workspace_size.argtypes = [i64, i64, i64, i64]
         _lib = lib
         return lib
 
@@ -149,6 +156,24 @@ def fa_fwd_ex_static(q: int, k: int, v: int, o: int, lse: int | None, B: int, H:
 
 def fa_fwd_ex_static_capacity() -> int:
     return int(load().fa_fwd_ex_static_capacity())
+
+
+def fa_bwd(q: int, k: int, v: int, o: int, dout: int, lse: int, dq: int, dk: int, dv: int, B: int,
+           H: int, H_kv: int, N_q: int, N_kv: int, d: int, scale: float, dtype: int,
+           workspace: int | None, workspace_bytes: int, stream: int | None) -> int:
+    return load().fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, N_q, N_kv, d, scale, dtype,
+                         workspace, workspace_bytes, stream)
+
+
+def fa_bwd_validate(q: int, k: int, v: int, o: int, dout: int, lse: int, dq: int, dk: int, dv: int,
+                    B: int, H: int, H_kv: int, N_q: int, N_kv: int, d: int, scale: float, dtype: int,
+                    workspace: int | None, workspace_bytes: int) -> int:
+    return load().fa_bwd_validate(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, N_q, N_kv, d, scale,
+                                  dtype, workspace, workspace_bytes)
+
+
+def fa_bwd_workspace_size(B: int, H: int, N_q: int, d: int) -> int:
+    return load().fa_bwd_workspace_size(B, H, N_q, d)
 
 
 def fa_device_status(stream: int | None) -> int:
@@ -219,3 +244,43 @@ def attention(q, k, v, scale: float | None = None, out=None, lse=None, with_lse:
     if st != FA_OK:
         raise FAError(st, "fa_fwd")
     return out, lse
+
+
+def attention_backward(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = False,
+                       dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of O = softmax(scale * Q K^T) V for CUDA
+    tensors q, o, dout [B, H, N_q, d] and k, v [B, H_kv, N_kv, d] (bf16 or
+    fp16), given the forward's o and fp32 lse [B, H, N_q].  scale defaults to
+    1/sqrt(d) in fp32.  `workspace` (uint8, at least fa_bwd_workspace_size
+    bytes) is allocated when not given.  Enqueued on `stream` (default:
+    PyTorch's current stream); raises FAError on a non-OK status."""
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape or o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError(f"incompatible shapes: q {q.shape} k {k.shape} v {v.shape} o {o.shape} "
+                         f"dout {dout.shape}")
+    for t in (q, k, v, o, dout, lse):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("every tensor must be a contiguous CUDA tensor")
+    if not (q.dtype == k.dtype == v.dtype == o.dtype == dout.dtype):
+        raise TypeError("q, k, v, o, dout must share a dtype")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != tuple(q.shape[:3]):
+        raise ValueError("lse must be fp32 [B, H, N_q]")
+    B, H, N_q, d = (int(x) for x in q.shape)
+    H_kv, N_kv = int(k.shape[1]), int(k.shape[2])
+    if scale is None:
+        scale = float(torch.tensor(1.0, dtype=torch.float32) / torch.sqrt(torch.tensor(float(d), dtype=torch.float32)))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = fa_bwd_workspace_size(B, H, N_q, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                    lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, H_kv, N_q, N_kv,
+                    d, float(scale), _dtype_code(q) | (FA_FLAG_CAUSAL if causal else 0),
+                    workspace.data_ptr(), workspace.numel() * workspace.element_size(), s.cuda_stream)
+    if st != FA_OK:
+        raise FAError(st, "fa_bwd")
+    return dq, dk, dv

@@ -18,20 +18,25 @@
 #include <cudaTypedefs.h>
 
 #include "fa.h"
+#include "fa_host.h"
 #include "fa_internal.h"
 
 // Set by the kernels when a bounded wait gives up (one per device).
 __device__ fa::DevStatus g_fa_device_status;
 
 namespace {
-
 thread_local char g_last_error[512] = "";
+}  // namespace
+
+namespace fa {
+namespace host {
 
 void set_error(const char* what, int code, const char* text) {
     std::snprintf(g_last_error, sizeof(g_last_error), "%s: error %d (%s)", what, code,
                   text ? text : "");
 }
 
+namespace {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 cudaError_t g_encode_err = cudaSuccess;
@@ -52,6 +57,7 @@ constexpr int kMaxDevices = 64;
 fa::DevStatus* g_err_ptr[kMaxDevices] = {};
 std::mutex g_err_mutex;
 std::atomic<unsigned int> g_generation{0};
+}  // namespace
 
 // Launch generation: never 0 (0 is the status word's initial abort_gen).
 unsigned int next_generation() {
@@ -89,11 +95,10 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
-// 3-D tiled map over [BH, N, d] (innermost first), 128-byte swizzle, boxes of
-// 128 bytes x box_rows rows x box_heads heads (128 x 1 normally; Nq x group
-// for packed grouped heads); rows past N read as zero and are not written.
+// Boxes are 128 x 1 rows x heads normally and Nq x group for packed grouped
+// heads in the forward pass.
 int encode_map(CUtensorMap* map, const void* base, int dtype, int64_t BH, int64_t N, int64_t d,
-               uint32_t box_rows = 128, uint32_t box_heads = 1) {
+               uint32_t box_rows, uint32_t box_heads) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (enc == nullptr) {
         set_error("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)",
@@ -121,6 +126,12 @@ int encode_map(CUtensorMap* map, const void* base, int dtype, int64_t BH, int64_
     return FA_OK;
 }
 
+}  // namespace host
+}  // namespace fa
+
+using namespace fa::host;
+
+namespace {
 constexpr int64_t kInt32Max = 2147483647;
 
 }  // namespace

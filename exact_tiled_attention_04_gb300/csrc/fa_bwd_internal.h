@@ -1,0 +1,81 @@
+// Declarations shared by the backward-pass entry points (fa_bwd_api.cu) and
+// its kernel translation units.  Not part of the public C ABI.
+//
+// The backward pass runs three kernels on the caller's stream:
+//   1. prep:  per query row i, D_i = dO_i . O_i and the negated base-2
+//             log-sum-exp -lse_i * log2(e) (the row statistics the main
+//             kernel reads), and a zeroed fp32 dQ accumulator row;
+//   2. main:  one CTA per 128 keys of one (batch, key/value head): dK and dV
+//             of those keys accumulated in tensor memory over every query
+//             tile of the head's query heads, and the dQ contribution of
+//             each (query tile, key block) pair added into the accumulator;
+//   3. dq:    dQ = scale * accumulator, converted to the input dtype.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+
+namespace fa {
+
+// Row statistics of one query row, as the main kernel reads them.
+struct RowStat {
+    float nlse2;  // -lse * log2(e), or -inf for a padding row or a row with no visible key
+    float D;      // sum_c dO[c] * O[c]; 0 for a padding row
+};
+
+// Parameters of the prep kernel.
+struct BwdPrepParams {
+    const void* o;        // [B*H, Nq, d] input dtype
+    const void* dout;     // [B*H, Nq, d] input dtype
+    const float* lse;     // [B*H, Nq] natural log
+    RowStat* stats;       // [B*H, Nq_pad]
+    float* dq_acc;        // [B*H, Nq, d] fp32, zeroed here
+    long long rows_pad;   // B*H*Nq_pad
+    int Nq;
+    int Nq_pad;           // Nq rounded up to a multiple of 128
+};
+
+// Parameters of one main-kernel launch, passed by value.
+struct BwdParams {
+    DevStatus* status;    // device status word of the current device
+    unsigned int gen;     // this launch's generation (never 0)
+    const RowStat* stats; // [B*H, Nq_pad]
+    float* dq_acc;        // [B*H, Nq, d] fp32 accumulator (reduced into)
+    int Nq;               // query rows per head
+    int Nkv;              // key / value rows per head
+    int Nq_pad;           // Nq rounded up to a multiple of 128
+    int n_q_tiles;        // Nq_pad / 128
+    int n_kv_blocks;      // ceil(Nkv / 128): CTAs per (batch, key/value head)
+    int H;                // query heads
+    int H_kv;             // key / value heads
+    int group;            // H / H_kv
+    int causal;           // 1: query i sees keys j <= i + causal_offset only
+    int causal_offset;    // Nkv - Nq
+    float scale_log2;     // scale * log2(e)
+    float scale;          // applied to dK in the epilogue
+};
+
+// Parameters of the dQ conversion.
+struct BwdDqParams {
+    const float* dq_acc;  // [n] fp32
+    void* dq;             // [n] input dtype
+    long long n;          // B*H*Nq*d (a multiple of 8)
+    float scale;
+};
+
+cudaError_t launch_bwd_prep(const BwdPrepParams& p, int d, int dtype, cudaStream_t stream);
+cudaError_t launch_bwd_dq(const BwdDqParams& p, int dtype, cudaStream_t stream);
+
+// Main kernel: grid = B * H_kv * n_kv_blocks CTAs of 384 threads.  Maps:
+// q, dO over [B*H, Nq, d]; k, v, dk, dv over [B*H_kv, Nkv, d].
+cudaError_t launch_bwd_bf16(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const CUtensorMap& dout, const CUtensorMap& dk, const CUtensorMap& dv,
+                            const BwdParams& p, unsigned int grid, cudaStream_t stream);
+cudaError_t launch_bwd_f16(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                           const CUtensorMap& dout, const CUtensorMap& dk, const CUtensorMap& dv,
+                           const BwdParams& p, unsigned int grid, cudaStream_t stream);
+
+}  // namespace fa

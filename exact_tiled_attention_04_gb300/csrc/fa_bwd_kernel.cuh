@@ -1,0 +1,573 @@
+// Backward pass of exact attention for sm_103a (GB300).
+//
+// What it computes: the gradients of O = softmax(scale Q K^T) V for an
+// upstream gradient dO, recomputing the attention blocks from Q, K, V and the
+// saved softmax statistic (lse) instead of storing the N x N matrix
+// ("FlashAttention dissected", section "Memory complexity: from O(N^2) to
+// O(N)"), with the exact gradient of the softmax formula of the same page:
+//   P = exp(scale S - lse),  dV = P^T dO,  dP = dO V^T,
+//   dS = P o (dP - D),  D_i = dO_i . O_i (= sum_j P_ij dP_ij),
+//   dQ = scale dS K,  dK = scale dS^T Q.
+//
+// Organisation (one CTA = 128 keys of one (batch, key/value head); it sweeps
+// every 128-row query tile of the head's query heads; 384 threads):
+//   warps 0-3  gradient warpgroup 0: query columns 0-63 of each tile
+//   warps 4-7  gradient warpgroup 1: query columns 64-127
+//   warp  8    tensor-core issuer (one thread) and TMEM owner
+//   warp  9    TMA producer (one thread)
+//   warps 10-11 idle (complete warpgroup 2 for the register reallocation)
+// Each thread of a gradient warpgroup owns one key row (its TMEM lane) and
+// half of the query columns.  The scores are computed transposed (keys on
+// the lanes) so that dK and dV accumulate in tensor memory for the whole
+// sweep, and P^T and dS^T are the A operands of their products straight
+// from tensor memory.
+//
+// Tensor memory (512 columns x 128 lanes, fp32):
+//   [0, 128)        S^T = K Q^T of the current tile.  Warpgroup w then
+//                   writes P^T (bf16/fp16 pairs) over its columns
+//                   [64w, 64w + 32) and dS^T over [64w + 32, 64w + 64).
+//   [128, 256)      dP^T = V dO^T; once dS is formed, the tile's dQ = dS K
+//                   (query rows on the lanes, d columns).
+//   [256, 256 + d)  dV accumulator;  [256 + d, 256 + 2d)  dK accumulator.
+// Per query tile the issuer enqueues S^T, dP^T (after the previous dQ was
+// read out), dV += P^T dO, then dK += dS^T Q and dQ = dS K.  The gradient
+// warpgroups add the tile's dQ into an fp32 accumulator in global memory
+// with vector reductions; a last kernel scales and converts it.
+//
+// Shared memory (128-byte-swizzled TMA tiles, 1024-byte aligned): K and V of
+// the key block (reused as the dK / dV output staging), a two-stage ring of
+// Q, dO and row-statistics tiles, and dS (128 keys x 128 queries, the
+// MN-major A operand of dQ = dS K).
+//
+// Every wait on an mbarrier is bounded as in the forward kernel: after about
+// a second the CTA raises its abort flag and the device error word, every
+// role leaves its loop, in-flight tensor-core work and TMA loads are
+// drained, and tensor memory is freed before the CTA exits.
+#pragma once
+
+#include <cmath>
+#include <cstdint>
+
+#include "fa_bwd_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+constexpr int kBwdThreads = 384;
+constexpr int kBwdMmaWarp = 8;
+constexpr int kBwdLoadWarp = 9;
+constexpr uint32_t kBwdLaunchRegs = 168;
+constexpr uint32_t kBwdTmemCols = 512;
+constexpr uint64_t kBwdWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+constexpr int kBwdStatBytes = 128 * static_cast<int>(sizeof(RowStat));  // one query tile
+
+template <int D, bool F16>
+struct BwdCfg {
+    static constexpr int kAtomElems = 64;                // 16-bit elements per 128-byte row
+    static constexpr int kAtoms = D / kAtomElems;
+    static constexpr int kAtomBytes = 128 * 128;         // 128 rows x 128 bytes
+    static constexpr int kTileBytes = kAtoms * kAtomBytes;  // 128 rows x D
+    static constexpr int kUmmaK = 16;
+    static constexpr int kDSteps = D / kUmmaK;           // k-steps of S^T and dP^T (over d)
+    static constexpr int kRowSteps = 128 / kUmmaK;       // k-steps over 128 query rows or keys
+    static constexpr int kStages = 2;
+    static constexpr uint32_t kFmt = F16 ? 0u : 1u;
+    // S^T = K Q^T and dP^T = V dO^T: M = 128 keys, N = 128 query rows, both K-major.
+    static constexpr uint32_t kIdescS = instr_desc(kFmt, false, false, 128, 128);
+    // dV += P^T dO and dK += dS^T Q: A from TMEM, B ([query rows x d]) MN-major.
+    static constexpr uint32_t kIdescAcc = instr_desc(kFmt, false, true, 128, D);
+    // dQ = dS K: A = dS (shared memory, stored keys x queries: MN-major),
+    // B = K ([keys x d]) MN-major; M = 128 query rows.
+    static constexpr uint32_t kIdescDQ = instr_desc(kFmt, true, true, 128, D);
+
+    // register split (setmaxnreg): gradient warpgroups / warpgroup 2
+    static constexpr uint32_t kGradRegs = 208;
+    static constexpr uint32_t kOtherRegs = 88;
+    static_assert(2 * 128 * kGradRegs + 128 * kOtherRegs == kBwdThreads * kBwdLaunchRegs,
+                  "register split must equal the launch allocation");
+
+    // shared-memory map (offsets from the 1024-aligned base)
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kOffK + kTileBytes;
+    static constexpr int kOffQ = kOffV + kTileBytes;                 // [kStages]
+    static constexpr int kOffDO = kOffQ + kStages * kTileBytes;      // [kStages]
+    static constexpr int kOffDS = kOffDO + kStages * kTileBytes;     // 128 x 128, two atoms
+    static constexpr int kOffStats = kOffDS + 2 * kAtomBytes;        // [kStages] x 1 KB
+    static constexpr int kTilesEnd = kOffStats + kStages * kBwdStatBytes;
+
+    // barrier slots
+    static constexpr int kBarKV = 0;
+    static constexpr int kBarFull = 1;                 // [kStages]
+    static constexpr int kBarEmpty = kBarFull + kStages;
+    static constexpr int kBarS = kBarEmpty + kStages;  // S^T computed
+    static constexpr int kBarDP = kBarS + 1;           // dP^T computed
+    static constexpr int kBarP = kBarDP + 1;           // P^T in TMEM (8 warp arrivals)
+    static constexpr int kBarDS = kBarP + 1;           // dS^T in TMEM and dS in smem (8)
+    static constexpr int kBarDQ = kBarDS + 1;          // dQ computed
+    static constexpr int kBarDQFree = kBarDQ + 1;      // dQ read out (8)
+    static constexpr int kBarAcc = kBarDQFree + 1;     // dK, dV final
+    static constexpr int kBarDrain = kBarAcc + 1;
+    static constexpr int kBarEpi = kBarDrain + 1;      // [2]
+    static constexpr int kNumBars = kBarEpi + 2;
+    // barriers, TMEM slot and abort flag
+    static constexpr int kCtrlBytes = kNumBars * 8 + 8;
+    // The control block lives in whichever alignment gap holds it: below the
+    // 1024-aligned base when the slack there is large enough, else after the
+    // tiles, so the launch needs only the tiles plus 1 KB.
+    static constexpr size_t kSmemBytes = static_cast<size_t>(kTilesEnd) + 1024;
+    static_assert(kCtrlBytes <= 512, "control block must fit either gap");
+    static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
+    static_assert(256 + 2 * D <= static_cast<int>(kBwdTmemCols), "tensor memory budget exceeded");
+};
+
+// Bounded wait on an mbarrier phase (the forward kernel's policy): returns
+// false when the CTA is aborting (if `honor_abort`) or when this wait gave up
+// after kBwdWaitLimitNs, in which case it raises the CTA's abort flag, sets
+// the sticky device error bits (waiting role in bits 8-15) and marks this
+// launch's generation as aborted.
+__device__ __forceinline__ bool bwd_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                         const BwdParams& bp, unsigned int where,
+                                         bool honor_abort = true) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    uint32_t spins = 0;
+    while (true) {
+        if (mbar_test(bar, parity)) return true;
+        if ((++spins & 31u) == 0u) {
+            if (honor_abort && *abort_flag) return false;
+            if (global_timer_ns() - t0 > kBwdWaitLimitNs) {
+                *abort_flag = 1u;
+                atomicOr(&bp.status->word, kDevErrTimeout | (where << 8));
+                atomicExch(&bp.status->abort_gen, bp.gen);
+                return false;
+            }
+        }
+    }
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from global memory into this CTA's
+// shared memory, completing on `bar` (transaction bytes).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// dst[0..3] += (a, b, c, d) in global memory (one 16-byte vector reduction).
+__device__ __forceinline__ void red_add_f32x4(float* dst, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ float bwd_u2f(uint32_t x) { return __uint_as_float(x); }
+
+template <int D, bool F16, bool kCausal>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                  const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
+                  const BwdParams p) {
+    using C = BwdCfg<D, F16>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_u32 & 1023u)) & 1023u;
+    uint8_t* smem = smem_raw + pad;
+    const uint32_t sbase = raw_u32 + pad;
+    // control block: below the aligned base if the slack holds it, else after the tiles
+    uint8_t* ctrl = (pad >= static_cast<uint32_t>(C::kCtrlBytes)) ? smem_raw : smem + C::kTilesEnd;
+    const uint32_t ctrl_u32 = smem_u32(ctrl);
+
+    const int warp = static_cast<int>(threadIdx.x) / 32;
+    const int lane = static_cast<int>(threadIdx.x) % 32;
+    // blockIdx.x = unit * n_kv_blocks + kb, unit = b * H_kv + key/value head
+    const int kb = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.n_kv_blocks));
+    const int unit = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.n_kv_blocks));
+    const int b = unit / p.H_kv;
+    const int kvh = unit % p.H_kv;
+    // Query tiles that see a key of this block: all, or under the causal mask
+    // those holding a row i >= kb*128 - causal_offset (query i sees key j iff
+    // j <= i + causal_offset).  The last query row sees every key, so at
+    // least one tile remains.
+    int qt_begin = 0;
+    if (kCausal) {
+        const long long first_i = static_cast<long long>(kb) * 128 - p.causal_offset;
+        qt_begin = first_i <= 0 ? 0 : static_cast<int>(min(first_i / 128, static_cast<long long>(p.n_q_tiles)));
+    }
+    const int nqt = p.n_q_tiles - qt_begin;
+    const int T = p.group * nqt;  // (query head, query tile) pairs swept by this CTA
+    const bool has_work = T > 0;
+
+    auto bar = [&](int i) -> uint32_t { return ctrl_u32 + 8u * static_cast<uint32_t>(i); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + C::kNumBars * 8);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(ctrl + C::kNumBars * 8 + 4);
+
+    // ---------------------------------------------------------------- setup
+    if (threadIdx.x == 0) {
+        mbar_init(bar(C::kBarKV), 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bar(C::kBarFull + s), 1);
+            mbar_init(bar(C::kBarEmpty + s), 1);
+        }
+        mbar_init(bar(C::kBarS), 1);
+        mbar_init(bar(C::kBarDP), 1);
+        mbar_init(bar(C::kBarP), 8);  // one arrival per gradient warp
+        mbar_init(bar(C::kBarDS), 8);
+        mbar_init(bar(C::kBarDQ), 1);
+        mbar_init(bar(C::kBarDQFree), 8);
+        mbar_init(bar(C::kBarAcc), 1);
+        mbar_init(bar(C::kBarDrain), 1);
+        mbar_init(bar(C::kBarEpi + 0), 128);
+        mbar_init(bar(C::kBarEpi + 1), 128);
+        // A CTA starting after another CTA of this launch timed out does no work.
+        *abort_flag = (*reinterpret_cast<volatile unsigned int*>(&p.status->abort_gen) == p.gen) ? 1u : 0u;
+        mbar_init_fence();
+    }
+    if (warp == kBwdLoadWarp && lane == 0) {
+        tma_prefetch_desc(&map_q);
+        tma_prefetch_desc(&map_k);
+        tma_prefetch_desc(&map_v);
+        tma_prefetch_desc(&map_do);
+    }
+    if (warp == kBwdMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), kBwdTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const bool skip = *abort_flag != 0u;
+
+    if (skip) {
+        // nothing issued: go straight to the teardown
+    } else if (warp >= 8) {
+        regs_decrease<C::kOtherRegs>();
+      if (!has_work) {
+        // no query row sees this key block: the epilogue stores zeros
+      } else if (warp == kBwdLoadWarp) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t keep = policy_evict_last();   // Q, dO, stats: read by every key block of the head
+            const uint64_t once = policy_evict_first();  // K, V: read once
+            mbar_arrive_expect_tx(bar(C::kBarKV), 2u * C::kTileBytes);
+            for (int a = 0; a < C::kAtoms; ++a) {
+                tma_load_3d(sbase + C::kOffK + a * C::kAtomBytes, &map_k, bar(C::kBarKV), a * C::kAtomElems,
+                            kb * 128, unit, once);
+                tma_load_3d(sbase + C::kOffV + a * C::kAtomBytes, &map_v, bar(C::kBarKV), a * C::kAtomElems,
+                            kb * 128, unit, once);
+            }
+            int issued = 0;
+            for (int it = 0; it < T; ++it) {
+                const int s = it % C::kStages;
+                if (!bwd_wait(bar(C::kBarEmpty + s), ((it / C::kStages) & 1) ^ 1, abort_flag, p, 31)) break;
+                const int g = it / nqt;
+                const int qt = qt_begin + it % nqt;
+                const int bh = b * p.H + kvh * p.group + g;
+                mbar_arrive_expect_tx(bar(C::kBarFull + s), 2u * C::kTileBytes + kBwdStatBytes);
+                for (int a = 0; a < C::kAtoms; ++a) {
+                    tma_load_3d(sbase + C::kOffQ + s * C::kTileBytes + a * C::kAtomBytes, &map_q,
+                                bar(C::kBarFull + s), a * C::kAtomElems, qt * 128, bh, keep);
+                    tma_load_3d(sbase + C::kOffDO + s * C::kTileBytes + a * C::kAtomBytes, &map_do,
+                                bar(C::kBarFull + s), a * C::kAtomElems, qt * 128, bh, keep);
+                }
+                bulk_load(sbase + C::kOffStats + s * kBwdStatBytes,
+                          p.stats + static_cast<size_t>(bh) * p.Nq_pad + static_cast<size_t>(qt) * 128,
+                          kBwdStatBytes, bar(C::kBarFull + s), keep);
+                issued = it + 1;
+            }
+            // Drain: every issued load has landed before the CTA may exit.
+            bwd_wait(bar(C::kBarKV), 0, abort_flag, p, 32, false);
+            for (int s = 0; s < C::kStages && s < issued; ++s) {
+                const int last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
+                bwd_wait(bar(C::kBarFull + s), (last / C::kStages) & 1, abort_flag, p, 32, false);
+            }
+        }
+      } else if (warp == kBwdMmaWarp) {
+        // ------------------------------------------------ tensor-core issuer
+        if (lane == 0) {
+            const uint32_t tS = tmem;             // S^T, then P^T / dS^T
+            const uint32_t tDP = tmem + 128u;     // dP^T, then dQ
+            const uint32_t tDV = tmem + 256u;
+            const uint32_t tDK = tmem + 256u + static_cast<uint32_t>(D);
+            const uint32_t sK = sbase + C::kOffK;
+            const uint32_t sV = sbase + C::kOffV;
+            const uint32_t sDS = sbase + C::kOffDS;
+            // K-major operand [128 rows x D]: a k-step is 16 elements (32 bytes)
+            auto kmaj = [&](uint32_t tile, int kk) {
+                const uint32_t off = (kk * 32) / 128 * C::kAtomBytes + (kk * 32) % 128;
+                return smem_desc_sw128(tile + off, 16, 1024);
+            };
+            // MN-major operand stored [rows x 128-byte rows]: a k-step is 16
+            // rows (2048 bytes); 64-element column blocks kAtomBytes apart
+            auto mnmaj = [&](uint32_t tile, int kk) {
+                return smem_desc_sw128(tile + kk * C::kUmmaK * 128, C::kAtomBytes, 1024);
+            };
+            bool ok = bwd_wait(bar(C::kBarKV), 0, abort_flag, p, 33);
+            for (int it = 0; ok && it < T; ++it) {
+                const int s = it % C::kStages;
+                ok = bwd_wait(bar(C::kBarFull + s), (it / C::kStages) & 1, abort_flag, p, 34);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t sQ = sbase + C::kOffQ + s * C::kTileBytes;
+                const uint32_t sDO = sbase + C::kOffDO + s * C::kTileBytes;
+                // S^T = K Q^T
+#pragma unroll
+                for (int kk = 0; kk < C::kDSteps; ++kk)
+                    mma_ss<false>(tS, kmaj(sK, kk), kmaj(sQ, kk), C::kIdescS, kk > 0 ? 1u : 0u);
+                tc_commit(bar(C::kBarS));
+                // dP^T = V dO^T, into the columns the previous tile's dQ occupied
+                if (it > 0) {
+                    ok = bwd_wait(bar(C::kBarDQFree), (it - 1) & 1, abort_flag, p, 35);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int kk = 0; kk < C::kDSteps; ++kk)
+                    mma_ss<false>(tDP, kmaj(sV, kk), kmaj(sDO, kk), C::kIdescS, kk > 0 ? 1u : 0u);
+                tc_commit(bar(C::kBarDP));
+                // dV += P^T dO: query rows 16kk.. of P^T sit in warpgroup kk/4's columns
+                ok = bwd_wait(bar(C::kBarP), it & 1, abort_flag, p, 36);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < C::kRowSteps; ++kk)
+                    mma_ts<false>(tDV, tS + (kk / 4) * 64 + (kk % 4) * 8, mnmaj(sDO, kk), C::kIdescAcc,
+                                  (it > 0 || kk > 0) ? 1u : 0u);
+                // dK += dS^T Q, then this tile's dQ = dS K
+                ok = bwd_wait(bar(C::kBarDS), it & 1, abort_flag, p, 37);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < C::kRowSteps; ++kk)
+                    mma_ts<false>(tDK, tS + (kk / 4) * 64 + 32 + (kk % 4) * 8, mnmaj(sQ, kk), C::kIdescAcc,
+                                  (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < C::kRowSteps; ++kk)
+                    mma_ss<false>(tDP, smem_desc_sw128(sDS + kk * C::kUmmaK * 128, C::kAtomBytes, 1024),
+                                  mnmaj(sK, kk), C::kIdescDQ, kk > 0 ? 1u : 0u);
+                tc_commit(bar(C::kBarDQ));
+                tc_commit(bar(C::kBarEmpty + s));  // Q, dO and stats of stage s are no longer read
+            }
+            if (ok) tc_commit(bar(C::kBarAcc));
+            // Drain every tensor-core operation before tensor memory is released.
+            tc_commit(bar(C::kBarDrain));
+            bwd_wait(bar(C::kBarDrain), 0, abort_flag, p, 38, false);
+        }
+      }
+    } else {
+        // ----------------------------------------------- gradient warpgroups
+        regs_increase<C::kGradRegs>();
+        const int w = warp / 4;         // query columns [64w, 64w + 64) of each tile
+        const int wi = warp % 4;        // TMEM lane quarter this warp may access
+        const int t = wi * 32 + lane;   // key row of the block (= TMEM lane); query row for dQ
+        const uint32_t lane_off = static_cast<uint32_t>(wi * 32) << 16;
+        const uint32_t tS = tmem + lane_off + 64u * static_cast<uint32_t>(w);
+        const uint32_t tDP = tmem + lane_off + 128u + 64u * static_cast<uint32_t>(w);
+        const uint32_t tDQ = tmem + lane_off + 128u + static_cast<uint32_t>(w * (D / 2));
+        const long long key = static_cast<long long>(kb) * 128 + t;
+        const bool key_valid = key < p.Nkv;  // rows past Nkv were zero-filled: weight 0
+        const float c = p.scale_log2;
+        bool ok = true;
+
+        for (int it = 0; it < T; ++it) {
+            const int s = it % C::kStages;
+            const int qt = qt_begin + it % nqt;
+            const int bh = b * p.H + kvh * p.group + it / nqt;
+            // the stage's statistics have landed, and S^T is ready
+            bool got = bwd_wait(bar(C::kBarFull + s), (it / C::kStages) & 1, abort_flag, p, 40);
+            if (got) got = bwd_wait(bar(C::kBarS), it & 1, abort_flag, p, 41);
+            ok = __all_sync(0xffffffffu, got);
+            if (!ok) break;
+            tc_fence_after();
+
+            uint32_t x[2][32];
+            tmem_ld32(tS, x[0]);
+            tmem_ld32(tS + 32u, x[1]);
+            tmem_ld_wait(x[0]);
+            tmem_ld_wait(x[1]);
+            // statistics of query columns 64w + 2m, 64w + 2m + 1: {nlse2, D, nlse2, D}
+            const float4* st4 = reinterpret_cast<const float4*>(smem + C::kOffStats + s * kBwdStatBytes) + 32 * w;
+            // causal: query column q (index qt*128 + q) sees this key iff q >= thr
+            int thr = 0;
+            if (kCausal) {
+                const long long v = key - p.causal_offset - static_cast<long long>(qt) * 128;
+                thr = static_cast<int>(v < -1 ? -1 : (v > 129 ? 129 : v));
+            }
+
+            // P^T = 2^(S^T scale log2(e) - lse_i log2(e)), kept in fp32 in x and
+            // written as 16-bit pairs over this warpgroup's first 32 columns
+            uint32_t pk[32];
+#pragma unroll
+            for (int m = 0; m < 32; ++m) {
+                const float4 st = st4[m];
+                const int h = m / 16, e = (m % 16) * 2;
+                float p0 = ex2(fmaf(bwd_u2f(x[h][e]), c, st.x));
+                float p1 = ex2(fmaf(bwd_u2f(x[h][e + 1]), c, st.z));
+                if (kCausal) {
+                    const int q0 = 64 * w + 2 * m;
+                    if (q0 < thr) p0 = 0.0f;
+                    if (q0 + 1 < thr) p1 = 0.0f;
+                }
+                if (!key_valid) {
+                    p0 = 0.0f;
+                    p1 = 0.0f;
+                }
+                x[h][e] = __float_as_uint(p0);
+                x[h][e + 1] = __float_as_uint(p1);
+                pk[m] = pack_16x2<F16>(p0, p1);
+            }
+            tmem_st32(tS, pk);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kBarP));
+
+            got = bwd_wait(bar(C::kBarDP), it & 1, abort_flag, p, 42);
+            ok = __all_sync(0xffffffffu, got);
+            if (!ok) break;
+            tc_fence_after();
+            // dS^T = P^T o (dP^T - D), written as 16-bit pairs over the next 32
+            // columns and, for dQ = dS K, into row t of shared-memory atom w
+            uint32_t dpk[32];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t dp[32];
+                tmem_ld32(tDP + 32u * h, dp);
+                tmem_ld_wait(dp);
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const int m = h * 16 + e / 2;
+                    const float4 st = st4[m];
+                    const float d0 = bwd_u2f(x[h][e]) * (bwd_u2f(dp[e]) - st.y);
+                    const float d1 = bwd_u2f(x[h][e + 1]) * (bwd_u2f(dp[e + 1]) - st.w);
+                    dpk[m] = pack_16x2<F16>(d0, d1);
+                }
+            }
+            tmem_st32(tS + 32u, dpk);
+            uint8_t* row_ptr = smem + C::kOffDS + w * C::kAtomBytes + t * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4*>(row_ptr + ((ch ^ (t & 7)) << 4)) =
+                    make_uint4(dpk[4 * ch], dpk[4 * ch + 1], dpk[4 * ch + 2], dpk[4 * ch + 3]);
+            fence_proxy_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kBarDS));
+
+            // this tile's dQ (query row t, columns [w d/2, (w+1) d/2)) into the
+            // fp32 accumulator
+            got = bwd_wait(bar(C::kBarDQ), it & 1, abort_flag, p, 43);
+            ok = __all_sync(0xffffffffu, got);
+            if (!ok) break;
+            tc_fence_after();
+            const long long qrow = static_cast<long long>(qt) * 128 + t;
+            float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + static_cast<size_t>(qrow)) * D + w * (D / 2);
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h) {
+                uint32_t v[32];
+                tmem_ld32(tDQ + 32u * h, v);
+                tmem_ld_wait(v);
+                if (qrow < p.Nq) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        red_add_f32x4(dst + 32 * h + e, bwd_u2f(v[e]), bwd_u2f(v[e + 1]), bwd_u2f(v[e + 2]),
+                                      bwd_u2f(v[e + 3]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kBarDQFree));
+        }
+
+        // ------------------------------------------------------- epilogue
+        // warpgroup 0: dV (staged in the V tile); warpgroup 1: scale * dK (in the K tile)
+        if (ok && has_work) {
+            const bool got = bwd_wait(bar(C::kBarAcc), 0, abort_flag, p, 44);
+            ok = __all_sync(0xffffffffu, got);
+        }
+        uint8_t* stage = smem + (w == 0 ? C::kOffV : C::kOffK);
+        if (ok) {
+            tc_fence_after();
+            const uint32_t tAcc = tmem + lane_off + 256u + (w == 0 ? 0u : static_cast<uint32_t>(D));
+            const float mul = (w == 0) ? 1.0f : p.scale;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t o[32];
+                if (has_work) {
+                    tmem_ld32(tAcc + 32u * q, o);
+                    tmem_ld_wait(o);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                }
+                // 32 values = half a swizzle row: chunks 4*(q%2) .. +3 of atom q/2
+                uint8_t* rowp = stage + (q / 2) * C::kAtomBytes + t * 128;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int ch = (q % 2) * 4 + cc;
+                    uint4 v4;
+                    v4.x = pack_16x2<F16>(bwd_u2f(o[8 * cc + 0]) * mul, bwd_u2f(o[8 * cc + 1]) * mul);
+                    v4.y = pack_16x2<F16>(bwd_u2f(o[8 * cc + 2]) * mul, bwd_u2f(o[8 * cc + 3]) * mul);
+                    v4.z = pack_16x2<F16>(bwd_u2f(o[8 * cc + 4]) * mul, bwd_u2f(o[8 * cc + 5]) * mul);
+                    v4.w = pack_16x2<F16>(bwd_u2f(o[8 * cc + 6]) * mul, bwd_u2f(o[8 * cc + 7]) * mul);
+                    *reinterpret_cast<uint4*>(rowp + ((ch ^ (t & 7)) << 4)) = v4;
+                }
+            }
+            fence_proxy_async_smem();
+        }
+        // Every thread of the warpgroup arrives exactly once, whatever happened.
+        mbar_arrive(bar(C::kBarEpi + w));
+        if (t == 0) {
+            const bool all_in = bwd_wait(bar(C::kBarEpi + w), 0, abort_flag, p, 45);
+            if (all_in && !*abort_flag) {
+                const CUtensorMap* map = (w == 0) ? &map_dv : &map_dk;
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_store_3d(map, smem_u32(stage + a * C::kAtomBytes), a * C::kAtomElems, kb * 128, unit);
+                tma_store_commit();
+                tma_store_wait_read();
+            }
+        }
+    }
+
+    // --------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kBwdMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kBwdTmemCols);
+    }
+}
+
+template <int D, bool F16, bool kCausal>
+cudaError_t launch_bwd_variant(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               const CUtensorMap& dout, const CUtensorMap& dk, const CUtensorMap& dv,
+                               const BwdParams& p, unsigned int grid, cudaStream_t stream) {
+    using C = BwdCfg<D, F16>;
+    auto kern = fa_bwd_kernel<D, F16, kCausal>;
+    // The register split relies on the compiled kernel holding exactly
+    // kBwdLaunchRegs per thread (a setmaxnreg.inc without the registers behind
+    // it would never return); refuse to launch otherwise.
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs != static_cast<int>(kBwdLaunchRegs)) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kBwdThreads, C::kSmemBytes, stream>>>(q, k, v, dout, dk, dv, p);
+    return cudaGetLastError();
+}
+
+template <int D, bool F16>
+cudaError_t launch_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                       const CUtensorMap& dout, const CUtensorMap& dk, const CUtensorMap& dv,
+                       const BwdParams& p, unsigned int grid, cudaStream_t stream) {
+    return p.causal ? launch_bwd_variant<D, F16, true>(q, k, v, dout, dk, dv, p, grid, stream)
+                    : launch_bwd_variant<D, F16, false>(q, k, v, dout, dk, dv, p, grid, stream);
+}
+
+}  // namespace fa

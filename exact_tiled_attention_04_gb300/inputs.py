@@ -35,7 +35,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 _CHUNK = 1 << 20  # pairs per chunk: bounds temporary memory
 
-TENSOR_Q, TENSOR_K, TENSOR_V, TENSOR_ROWS = 0, 1, 2, 3
+TENSOR_Q, TENSOR_K, TENSOR_V, TENSOR_ROWS, TENSOR_DO = 0, 1, 2, 3, 4
 
 
 def mix64(z: np.ndarray) -> np.ndarray:
@@ -293,3 +293,11 @@ def make_general(B: int, H: int, H_kv: int, Nq: int, Nkv: int, d: int, dtype: st
         n = shape[0] * shape[1] * shape[2] * shape[3]
         out.append(_finish(normals(seed, t, n, factor).reshape(shape), dtype))
     return tuple(out)
+
+
+def make_dout(B: int, H: int, Nq: int, d: int, dtype: str = "bf16", seed: int = 13,
+              factor: float = 1.0) -> np.ndarray:
+    """Seeded upstream gradient dO [B, H, Nq, d] for the backward pass, drawn
+    like the inputs (its own counter stream) and rounded to the dtype."""
+    n = B * H * Nq * d
+    return _finish(normals(seed, TENSOR_DO, n, factor).reshape(B, H, Nq, d), dtype)

@@ -178,6 +178,55 @@ int fa_fwd_ex_static(const void* q, const void* k, const void* v, void* o,
 size_t fa_fwd_ex_static_capacity(void);
 
 /*
+ * fa_bwd — gradients of exact attention for an upstream gradient dO:
+ *
+ *   P = softmax(scale Q K^T) (recomputed from q, k and the saved lse),
+ *   dV = P^T dO,  dS = P o (dO V^T - D),  D_i = dO_i . O_i,
+ *   dQ = scale dS K,  dK = scale dS^T Q.
+ *
+ * "FlashAttention dissected", section "Memory complexity: from O(N^2) to
+ * O(N)": the backward pass recomputes the attention blocks from Q, K, V and
+ * the saved softmax statistics instead of storing the N x N matrix; the
+ * gradient is the exact one of the forward definition (the pages give no
+ * formula; this is the chain rule through O = P V and the softmax formula of
+ * the same page).  The causal mask and grouped heads are those of fa_fwd_ex.
+ *
+ * Layout (contiguous, row-major, dtype = the inputs' dtype):
+ *   q, o, dout, dq : [B, H, N_q, d]      k, v, dk, dv : [B, H_kv, N_kv, d]
+ *   lse            : fp32 [B, H, N_q], natural log, as fa_fwd / fa_fwd_ex
+ *                    return it (a row with no visible key: -inf)
+ *   o and lse must be the forward outputs for the same q, k, v, scale and
+ *   mask; dk and dv sum over the H / H_kv query heads sharing a key/value
+ *   head.
+ * dtype: FA_DTYPE_BF16 or FA_DTYPE_F16, optionally | FA_FLAG_CAUSAL;
+ *   FA_DTYPE_F32 returns FA_ERR_UNSUPPORTED.  d: 64 or 128.
+ * workspace: caller-owned device memory of at least
+ *   fa_bwd_workspace_size(B, H, N_q, d) bytes, 16-byte aligned (fp32 row
+ *   statistics and the fp32 dQ accumulator; nothing needs to be zeroed).
+ * Ownership and errors: as fa_fwd_ex.  Every pointer must be non-NULL and
+ *   16-byte aligned (lse 4-byte); dq, dk, dv and the workspace must not
+ *   overlap any input or one another (inputs may alias one another).
+ *   Validation failures return before any CUDA call.  Three kernels are
+ *   enqueued on `stream`; the call does not wait for them.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o,
+           const void* dout, const float* lse, void* dq, void* dk, void* dv,
+           int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv,
+           int64_t d, float scale, int dtype, void* workspace,
+           size_t workspace_bytes, void* stream);
+
+/* The argument checks of fa_bwd alone; never touches the GPU. */
+int fa_bwd_validate(const void* q, const void* k, const void* v, const void* o,
+                    const void* dout, const float* lse, void* dq, void* dk,
+                    void* dv, int64_t B, int64_t H, int64_t H_kv, int64_t N_q,
+                    int64_t N_kv, int64_t d, float scale, int dtype,
+                    const void* workspace, size_t workspace_bytes);
+
+/* Workspace bytes fa_bwd needs (0 for invalid sizes):
+   8 * B * H * ceil(N_q / 128) * 128 (rounded up to 256) + 4 * B * H * N_q * d. */
+size_t fa_bwd_workspace_size(int64_t B, int64_t H, int64_t N_q, int64_t d);
+
+/*
  * fa_device_status — synchronise `stream`, then read and clear the device
  * error word the kernels set when a bounded wait gives up.  Returns FA_OK,
  * FA_ERR_TIMEOUT, or FA_ERR_CUDA if the synchronisation itself failed.

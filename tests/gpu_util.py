@@ -165,3 +165,58 @@ def compare_ex(dtype: str, o_gpu, lse_gpu, q, k, v, scale=None, rows=None, causa
 
 def tol_o_dtype(dtype: str) -> float:
     return {"bf16": TOL_O_BF16, "f16": TOL_O_F16, "f32": TOL_O_F32}[dtype]
+
+
+# Backward pass: error = max |g - g_ref| / max |g_ref| per gradient tensor.
+# P and dS are rounded to the input dtype before their products (relative
+# 2^-9 for bf16, 2^-12 for fp16) and the outputs once more; each gradient
+# element sums many such terms with independent rounding errors, so the
+# normalised error stays near one output rounding (2^-9 = 2e-3 for bf16,
+# 2^-12 = 2.4e-4 for fp16).  The bars leave 5x and 10x room for the D_i
+# formed from the rounded forward output and for fp32 accumulation order.
+TOL_GRAD_BF16 = 1e-2
+TOL_GRAD_F16 = 2.5e-3
+
+
+def tol_grad(dtype: str) -> float:
+    return TOL_GRAD_F16 if dtype == "f16" else TOL_GRAD_BF16
+
+
+def run_bwd(q, k, v, dout, dtype: str, causal: bool = False, scale=None):
+    """Forward (fa_fwd_ex, one partition) then fa_bwd on the GPU through the
+    C ABI; returns (dq, dk, dv) as float32 numpy arrays and the scale used.
+    Outputs and workspace are poisoned with NaN first."""
+    import torch
+    B, H, Nq, d = q.shape
+    H_kv, Nkv = k.shape[1], k.shape[2]
+    sc = float(np.float32(1.0 / np.sqrt(d))) if scale is None else float(scale)
+    tq, tk, tv, tdo = (to_device(x, dtype) for x in (q, k, v, dout))
+    o = torch.full_like(tq, float("nan"))
+    lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    code = DTYPE_CODES[dtype] | (fab.FA_FLAG_CAUSAL if causal else 0)
+    st = fab.fa_fwd_ex(tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, H_kv,
+                       Nq, Nkv, d, sc, code, 1, None, 0, s)
+    assert st == fab.FA_OK, (st, fab.fa_last_error_message())
+    dq = torch.full_like(tq, float("nan"))
+    dk = torch.full_like(tk, float("nan"))
+    dv = torch.full_like(tv, float("nan"))
+    need = fab.fa_bwd_workspace_size(B, H, Nq, d)
+    ws = torch.full((need // 4,), float("nan"), dtype=torch.float32, device="cuda")
+    st = fab.fa_bwd(tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), o.data_ptr(), tdo.data_ptr(), lse.data_ptr(),
+                    dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, H_kv, Nq, Nkv, d, sc, code,
+                    ws.data_ptr(), need, s)
+    assert st == fab.FA_OK, (st, fab.fa_last_error_message())
+    st = fab.fa_device_status(s)
+    assert st == fab.FA_OK, (st, fab.fa_status_string(st), fab.fa_last_error_message())
+    return (dq.float().cpu().numpy(), dk.float().cpu().numpy(), dv.float().cpu().numpy()), sc
+
+
+def grad_errors(got, ref):
+    """Normalised errors (max |g - ref| / max |ref|) of (dq, dk, dv)."""
+    out = []
+    for g, r in zip(got, ref):
+        assert np.isfinite(g).all()
+        den = max(float(np.max(np.abs(r))), 1e-30)
+        out.append(float(np.max(np.abs(g.astype(np.float64) - r))) / den)
+    return out

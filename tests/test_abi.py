@@ -145,3 +145,38 @@ def test_dtype_flags(lib):
     assert validate(dtype=fab.FA_DTYPE_BF16 | fab.FA_FLAG_CAUSAL) == fab.FA_OK
     assert validate(dtype=fab.FA_DTYPE_BF16 | 0x200) == fab.FA_ERR_INVALID_ARG  # unknown flag
     assert validate_ex(dtype=fab.FA_DTYPE_F16 | fab.FA_FLAG_CAUSAL) == fab.FA_OK
+
+
+def validate_bwd(q=Q, k=K, v=V, o=O, dout=6 << 32, lse=L, dq=7 << 32, dk=8 << 32, dv=9 << 32, B=2, H=8,
+                 H_kv=2, Nq=300, Nkv=333, d=64, scale=0.125, dtype=fab.FA_DTYPE_BF16, ws=10 << 32,
+                 wbytes=None):
+    if wbytes is None:
+        wbytes = fab.fa_bwd_workspace_size(B, H, Nq, d)
+    return fab.fa_bwd_validate(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, Nq, Nkv, d, scale, dtype,
+                               ws, wbytes)
+
+
+def test_bwd_validation(lib):
+    # statistics: 8 bytes per padded query row (3 tiles of 128), then fp32 dQ
+    assert fab.fa_bwd_workspace_size(2, 8, 300, 64) == 2 * 8 * 384 * 8 + 2 * 8 * 300 * 64 * 4
+    assert fab.fa_bwd_workspace_size(1, 1, 1, 96) == 0
+    assert validate_bwd() == fab.FA_OK
+    assert validate_bwd(dtype=fab.FA_DTYPE_F16 | fab.FA_FLAG_CAUSAL, d=128) == fab.FA_OK
+    assert validate_bwd(dtype=fab.FA_DTYPE_F32) == fab.FA_ERR_UNSUPPORTED
+    assert validate_bwd(d=96) == fab.FA_ERR_UNSUPPORTED
+    assert validate_bwd(dtype=fab.FA_DTYPE_BF16 | 0x200) == fab.FA_ERR_INVALID_ARG
+    assert validate_bwd(H_kv=3) == fab.FA_ERR_INVALID_ARG
+    assert validate_bwd(lse=None) == fab.FA_ERR_INVALID_ARG
+    assert validate_bwd(ws=None) == fab.FA_ERR_INVALID_ARG
+    assert validate_bwd(wbytes=fab.fa_bwd_workspace_size(2, 8, 300, 64) - 1) == fab.FA_ERR_INVALID_ARG
+    assert validate_bwd(dq=(7 << 32) + 8) == fab.FA_ERR_ALIGNMENT
+    assert validate_bwd(ws=(10 << 32) + 4) == fab.FA_ERR_ALIGNMENT
+    assert validate_bwd(lse=L + 2) == fab.FA_ERR_ALIGNMENT
+    assert validate_bwd(dk=Q + 64) == fab.FA_ERR_INVALID_ARG     # output overlaps an input
+    assert validate_bwd(dv=8 << 32) == fab.FA_ERR_INVALID_ARG    # dv overlaps dk
+    assert validate_bwd(ws=O) == fab.FA_ERR_INVALID_ARG          # workspace overlaps o
+    assert validate_bwd(scale=float("nan")) == fab.FA_ERR_INVALID_ARG
+    assert validate_bwd(k=Q, v=Q) == fab.FA_OK                   # inputs may alias
+    # rejected before any CUDA call
+    assert fab.fa_bwd(Q, K, V, O, 6 << 32, L, 7 << 32, 8 << 32, 9 << 32, 2, 8, 2, 300, 333, 96, 0.125,
+                      fab.FA_DTYPE_BF16, 10 << 32, 1 << 30, None) == fab.FA_ERR_UNSUPPORTED
