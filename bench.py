@@ -4,7 +4,9 @@
                     [--workload NAME]
 
 One step = one fa_fwd call over the whole workload (every (batch, head) and
-every query row): the complete hot path.  Default workload: B=2, H=32,
+every query row): the complete hot path.  Backward workloads (bwd_*): one
+step = one fa_bwd call (dQ, dK, dV for a seeded dO, three kernels) on the
+forward outputs computed once before timing; 10*B*H*N^2*d flops per step.  Default workload: B=2, H=32,
 N=8192, d=128, bf16 inputs drawn N(0,1)*0.5 from a seed (the compute-bound
 headline shape).  The metric is attention-forward TFLOP/s counting
 4*B*H*N^2*d flops per step.
@@ -28,6 +30,7 @@ there is) on bounded samples of the workload and prints the same line with
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -42,6 +45,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s (4·B·H·N²·d) on 1 GB300 and % of dense tensor peak"
+METRIC_BWD = "attention bwd TFLOP/s (10·B·H·N²·d) on 1 GB300 and % of dense tensor peak"
 UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
@@ -91,21 +95,25 @@ def measured_peaks():
         return None
 
 
-def kernel_source_hash() -> str:
-    """Hash of the forward path's CUDA sources (every file of csrc/ except
-    the backward pass's fa_bwd*): ties a stored ncu traffic figure to the
-    kernel it was measured on."""
+BWD_SHARED = ("fa_ptx.cuh", "fa_internal.h", "fa_host.h")
+
+
+def kernel_source_hash(backward: bool = False) -> str:
+    """Hash of the CUDA sources a pass is built from: ties a stored ncu
+    traffic figure to the kernel it was measured on.  Forward: every file of
+    csrc/ except the backward pass's fa_bwd*; backward: the fa_bwd* files
+    and the headers they share with the forward pass."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_tiled_attention_04_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.startswith("fa_bwd"):
-            continue
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        is_bwd = name.startswith("fa_bwd")
+        if (is_bwd or name in BWD_SHARED) if backward else not is_bwd:
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
-def stored_traffic(workload: str):
+def stored_traffic(workload: str, backward: bool = False):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel sources; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
@@ -114,7 +122,7 @@ def stored_traffic(workload: str):
             lines = [ln.strip() for ln in f if ln.strip() and not ln.startswith("#")]
     except OSError:
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(backward)
     for ln in lines:
         kv = dict(x.split("=", 1) for x in ln.split() if "=" in x)
         if kv.get("workload") == workload and kv.get("kernel_hash") == want:
@@ -187,7 +195,7 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- CPU oracle
-def cpu_oracle_rate(w, q, k, v, target_s: float, max_rows: int | None = None):
+def cpu_oracle_rate(w, q, k, v, dout, target_s: float, max_rows: int | None = None):
     """Time the fp64 oracle on seeded rows of the workload, sized to run
     about `target_s` seconds on every host core.  Returns (TFLOP/s, cores,
     rows, seconds)."""
@@ -196,25 +204,42 @@ def cpu_oracle_rate(w, q, k, v, target_s: float, max_rows: int | None = None):
     cores = oracle.default_threads()
     rows = I.sample_rows(w, 64, seed_offset=1000)
     t0 = time.perf_counter()
-    oracle.attention_f64_ex(q, k, v, float(w.scale), rows=rows, causal=w.causal)
+    oracle_rows(w, q, k, v, dout, rows)
     dt = max(time.perf_counter() - t0, 1e-6)
     n = int(64 * target_s / dt)
     n = max(cores, min(n, max_rows or n, w.B * w.H * w.N))
     rows = I.sample_rows(w, n, seed_offset=1001)
     t0 = time.perf_counter()
-    oracle.attention_f64_ex(q, k, v, float(w.scale), rows=rows, causal=w.causal)
+    oracle_rows(w, q, k, v, dout, rows)
     dt = time.perf_counter() - t0
     return row_flops(w, rows) / dt / 1e12, cores, n, dt
 
 
 def row_flops(w, rows) -> float:
-    """Algorithmic flops of the given (b, h, i) query rows: 4 d per visible key."""
+    """Flops the oracle spends on the given (b, h, i) query rows: forward,
+    4 d per visible key (scores, weighted sum of V); backward (dQ of the
+    row), 6 d per visible key (scores, dP, dS K)."""
     import numpy as np
     i = np.asarray(rows)[:, 2].astype(np.float64)
     visible = np.full_like(i, float(w.Nkv))
     if w.causal:
         visible = np.clip(i + (w.Nkv - w.N) + 1, 0, w.Nkv)
-    return float(4.0 * w.d * visible.sum())
+    return float((6.0 if w.backward else 4.0) * w.d * visible.sum())
+
+
+def oracle_rows(w, q, k, v, dout, rows):
+    """The oracle on sampled query rows: the forward (O, lse) or, for a
+    backward workload, the rows' dQ."""
+    import oracle
+    if w.backward:
+        return oracle.attention_bwd_dq_rows_f64(q, k, v, dout, float(w.scale), rows, causal=w.causal)
+    return oracle.attention_f64_ex(q, k, v, float(w.scale), rows=rows, causal=w.causal)
+
+
+def sample_text(w, n, cores, secs=None):
+    what = ("dQ of" if w.backward else "") + f" {n} seeded query rows of the workload (of {w.B * w.H * w.N})"
+    how = "fp64, recomputed softmax" if w.backward else "fp64 three-pass"
+    return what.strip() + f", {how}, {cores} threads" + (f", {secs:.1f} s" if secs is not None else "")
 
 
 # ------------------------------------------------------------------- arms
@@ -227,27 +252,27 @@ def run_reference(args, w):
     import oracle
     from exact_tiled_attention_04_gb300 import inputs as I
     q, k, v = I.make(w)
+    dout = I.make_dout(w.B, w.H, w.N, w.d, w.dtype, seed=w.seed) if w.backward else None
     cores = oracle.default_threads()
     budget_s = 150.0 / max(1, args.steps + args.warmup)
     rows = I.sample_rows(w, 16, seed_offset=2000)
     t0 = time.perf_counter()
-    oracle.attention_f64_ex(q, k, v, float(w.scale), rows=rows, causal=w.causal)
+    oracle_rows(w, q, k, v, dout, rows)
     per_row = max((time.perf_counter() - t0) / 16, 1e-7)
     n = int(max(1, min(4096, w.B * w.H * w.N, budget_s / per_row)))
     for i in range(args.warmup):
-        oracle.attention_f64_ex(q, k, v, float(w.scale), rows=I.sample_rows(w, n, seed_offset=3000 + i),
-                                causal=w.causal)
+        oracle_rows(w, q, k, v, dout, I.sample_rows(w, n, seed_offset=3000 + i))
     total = 0.0
     t0 = time.perf_counter()
     for i in range(args.steps):
         rows = I.sample_rows(w, n, seed_offset=4000 + i)
-        oracle.attention_f64_ex(q, k, v, float(w.scale), rows=rows, causal=w.causal)
+        oracle_rows(w, q, k, v, dout, rows)
         total += row_flops(w, rows)
     dt = time.perf_counter() - t0
     value = total / dt / 1e12
-    sample = f"{n} seeded query rows of the workload per step (of {w.B * w.H * w.N}), fp64, {cores} threads"
+    sample = sample_text(w, n, cores) + " per step"
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC_BWD if w.backward else METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
@@ -272,6 +297,8 @@ def config_of(w, n_gpus: int, splits: int = 1):
         cfg["causal"] = True
     if splits > 1:
         cfg["splits"] = splits
+    if w.backward:
+        cfg["pass"] = "backward: dQ, dK, dV for a seeded dO (forward outputs o, lse computed once)"
     return cfg
 
 
@@ -288,9 +315,7 @@ def run_ours(args, w):
     fab.load()
 
     # per-rank inputs (weak scaling: every rank its own seeded copy)
-    wr = I.Workload(w.name, w.B, w.H, w.N, w.d, w.dtype, w.seed + 17 * rank, w.factor,
-                    w.identical_k_heads, w.q_scaled_heads, w.oracle_rows, w.note, w.H_kv, w.Nkv,
-                    w.causal, w.splits)
+    wr = dataclasses.replace(w, seed=w.seed + 17 * rank)
     q, k, v = I.make(wr)
 
     def host_tensor(x):
@@ -316,16 +341,51 @@ def run_ours(args, w):
         splits = fab.fa_fwd_ex_splits(w.B, w.H, w.H_kv, w.N, w.Nkv, sms)
     wbytes = fab.fa_fwd_ex_workspace_size(w.B, w.H, w.N, w.Nkv, w.d, splits)
     work = torch.empty(max(wbytes, 16), dtype=torch.uint8, device=dev)  # caller-owned scratch
-    kernels_per_step = 2 if wbytes else 1  # forward (+ merge of the partitions)
     launches = 0
 
-    def step():
-        nonlocal launches
+    def forward():
         st = fab.fa_fwd_ex(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), do.data_ptr(), dlse.data_ptr(),
                            w.B, w.H, w.H_kv, w.N, w.Nkv, w.d, scale, dt_code, splits,
                            work.data_ptr() if wbytes else None, wbytes, sp)
         if st != fab.FA_OK:
             raise fab.FAError(st, "fa_fwd_ex")
+
+    if not w.backward:
+        kernels_per_step = 2 if wbytes else 1  # forward (+ merge of the partitions)
+        step_fn = forward
+        # end to end: q, k, v up; o and lse back
+        h2d_pairs = [(dq, hq), (dk, hk), (dv, hv)]
+        ho = torch.empty_like(hq).pin_memory()
+        hl = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+        d2h_pairs = [(ho, do), (hl, dlse)]
+    else:
+        # the forward outputs o, lse the backward consumes, computed once
+        with torch.cuda.stream(stream):
+            forward()
+        torch.cuda.synchronize(dev)
+        hdout = host_tensor(I.make_dout(w.B, w.H, w.N, w.d, w.dtype, seed=wr.seed)).pin_memory()
+        ddout = hdout.to(dev)
+        ho, hl = do.cpu().pin_memory(), dlse.cpu().pin_memory()
+        gq, gk, gv = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
+        bwd_bytes = fab.fa_bwd_workspace_size(w.B, w.H, w.N, w.d)
+        bwork = torch.empty(bwd_bytes, dtype=torch.uint8, device=dev)
+        kernels_per_step = 3  # prep, main, dQ conversion
+
+        def step_fn():
+            st = fab.fa_bwd(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), do.data_ptr(), ddout.data_ptr(),
+                            dlse.data_ptr(), gq.data_ptr(), gk.data_ptr(), gv.data_ptr(), w.B, w.H, w.H_kv,
+                            w.N, w.Nkv, w.d, scale, dt_code, bwork.data_ptr(), bwd_bytes, sp)
+            if st != fab.FA_OK:
+                raise fab.FAError(st, "fa_bwd")
+
+        # end to end: q, k, v, o, dO, lse up; dq, dk, dv back
+        h2d_pairs = [(dq, hq), (dk, hk), (dv, hv), (do, ho), (ddout, hdout), (dlse, hl)]
+        hgq, hgk, hgv = (torch.empty_like(t).pin_memory() for t in (hq, hk, hv))
+        d2h_pairs = [(hgq, gq), (hgk, gk), (hgv, gv)]
+
+    def step():
+        nonlocal launches
+        step_fn()
         launches += kernels_per_step
 
     torch.cuda.synchronize(dev)
@@ -365,10 +425,8 @@ def run_ours(args, w):
 
     # ---- end to end: host copies inside the timed region
     e2e_steps = max(3, min(args.steps, 20))
-    ho = torch.empty_like(hq).pin_memory()
-    hl = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    h2d = sum(h.numel() * h.element_size() for _, h in h2d_pairs)
+    d2h = sum(h.numel() * h.element_size() for h, _ in d2h_pairs)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -376,12 +434,11 @@ def run_ours(args, w):
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(e2e_steps):
-            dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-            step()
-            ho.copy_(do, non_blocking=True)
-            hl.copy_(dlse, non_blocking=True)
+            for dst, src in h2d_pairs:
+                dst.copy_(src, non_blocking=True)
+            step_fn()
+            for dst, src in d2h_pairs:
+                dst.copy_(src, non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = reduce_max(e0.elapsed_time(e1), dist, dev)
@@ -408,8 +465,12 @@ def run_ours(args, w):
     step_s = kernel_ms * 1e-3
     intensity = w.flops() / w.bytes()
     ridge = tensor_peak * 1e12 / (hbm_peak * 1e9)
-    kernel_name = (f"fa_fwd_kernel<{w.dtype},{w.d}{',causal' if w.causal else ''}>"
-                   + (" + fa_merge_kernel" if kernels_per_step == 2 else ""))
+    if w.backward:
+        kernel_name = (f"fa_bwd_kernel<{w.dtype},{w.d}{',causal' if w.causal else ''}> + fa_bwd_prep_kernel"
+                       " + fa_bwd_dq_kernel (timed as the whole step)")
+    else:
+        kernel_name = (f"fa_fwd_kernel<{w.dtype},{w.d}{',causal' if w.causal else ''}>"
+                       + (" + fa_merge_kernel" if kernels_per_step == 2 else ""))
     if intensity >= ridge:
         achieved = w.flops() / step_s / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": UNIT,
@@ -419,14 +480,15 @@ def run_ours(args, w):
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                     "frac": achieved / hbm_peak,
                     "peak_source": "measured copy bandwidth (MEASURED_PEAKS.json)" if peaks else "fallback"}
-    roofline.update({"traffic": stored_traffic(w.name), "kernel": kernel_name,
+    roofline.update({"traffic": stored_traffic(w.name, w.backward), "kernel": kernel_name,
                      "algorithmic_flops_per_launch": w.flops(),
                      "algorithmic_bytes_per_launch": w.bytes(),
                      "arithmetic_intensity": intensity})
     frac_tensor = value / world / tensor_peak
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC_BWD if w.backward else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": config_of(w, world, splits),
@@ -438,10 +500,10 @@ def run_ours(args, w):
         "clocks": {k2: clk[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
     }
     if world == 1 and not args.no_cpu_baseline:
-        rate, cores, n, secs = cpu_oracle_rate(wr, q, k, v, target_s=args.cpu_seconds)
+        dout_np = I.make_dout(w.B, w.H, w.N, w.d, w.dtype, seed=wr.seed) if w.backward else None
+        rate, cores, n, secs = cpu_oracle_rate(wr, q, k, v, dout_np, target_s=args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"{n} seeded query rows of the workload "
-                                          f"(of {w.B * w.H * w.N}), fp64 three-pass, {secs:.1f} s"}
+                                "sample": sample_text(w, n, cores, secs)}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

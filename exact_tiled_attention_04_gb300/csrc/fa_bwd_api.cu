@@ -87,7 +87,7 @@ int launch_bwd_all(const void* q, const void* k, const void* v, const void* o, c
     const bool causal = (dtype_arg & FA_FLAG_CAUSAL) != 0;
     const int64_t BH = B * H, BHkv = B * H_kv;
     const int64_t Nq_pad = pad128(N_q);
-    CUtensorMap mq, mk, mv, mdo, mdk, mdv;
+    CUtensorMap mq, mk, mv, mdo, mdk, mdv, mdq;
     int st;
     if ((st = encode_map(&mq, q, dtype, BH, N_q, d)) != FA_OK) return st;
     if ((st = encode_map(&mdo, dout, dtype, BH, N_q, d)) != FA_OK) return st;
@@ -99,6 +99,7 @@ int launch_bwd_all(const void* q, const void* k, const void* v, const void* o, c
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     fa::RowStat* stats = reinterpret_cast<fa::RowStat*>(ws);
     float* dq_acc = reinterpret_cast<float*>(ws + stats_bytes(B, H, N_q));
+    if ((st = encode_map(&mdq, dq_acc, FA_DTYPE_F32, BH, N_q, d)) != FA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     fa::BwdPrepParams pp{};
@@ -121,7 +122,6 @@ int launch_bwd_all(const void* q, const void* k, const void* v, const void* o, c
     if (st != FA_OK) return st;
     p.gen = next_generation();
     p.stats = stats;
-    p.dq_acc = dq_acc;
     p.Nq = static_cast<int>(N_q);
     p.Nkv = static_cast<int>(N_kv);
     p.Nq_pad = static_cast<int>(Nq_pad);
@@ -136,8 +136,8 @@ int launch_bwd_all(const void* q, const void* k, const void* v, const void* o, c
     p.scale = scale;
     const unsigned int grid = static_cast<unsigned int>(BHkv * p.n_kv_blocks);
     e = (dtype == FA_DTYPE_BF16)
-            ? fa::launch_bwd_bf16(static_cast<int>(d), mq, mk, mv, mdo, mdk, mdv, p, grid, s)
-            : fa::launch_bwd_f16(static_cast<int>(d), mq, mk, mv, mdo, mdk, mdv, p, grid, s);
+            ? fa::launch_bwd_bf16(static_cast<int>(d), mq, mk, mv, mdo, mdk, mdv, mdq, p, grid, s)
+            : fa::launch_bwd_f16(static_cast<int>(d), mq, mk, mv, mdo, mdk, mdv, mdq, p, grid, s);
     if (e != cudaSuccess) {
         set_error("backward kernel launch", static_cast<int>(e), cudaGetErrorString(e));
         return FA_ERR_CUDA;

@@ -5,9 +5,10 @@ namespace fa {
 
 cudaError_t launch_bwd_f16(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                            const CUtensorMap& dout, const CUtensorMap& dk, const CUtensorMap& dv,
-                           const BwdParams& p, unsigned int grid, cudaStream_t stream) {
-    if (d == 64) return launch_bwd<64, true>(q, k, v, dout, dk, dv, p, grid, stream);
-    if (d == 128) return launch_bwd<128, true>(q, k, v, dout, dk, dv, p, grid, stream);
+                           const CUtensorMap& dq, const BwdParams& p, unsigned int grid,
+                           cudaStream_t stream) {
+    if (d == 64) return launch_bwd<64, true>(q, k, v, dout, dk, dv, dq, p, grid, stream);
+    if (d == 128) return launch_bwd<128, true>(q, k, v, dout, dk, dv, dq, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -43,7 +43,6 @@ struct BwdParams {
     DevStatus* status;    // device status word of the current device
     unsigned int gen;     // this launch's generation (never 0)
     const RowStat* stats; // [B*H, Nq_pad]
-    float* dq_acc;        // [B*H, Nq, d] fp32 accumulator (reduced into)
     int Nq;               // query rows per head
     int Nkv;              // key / value rows per head
     int Nq_pad;           // Nq rounded up to a multiple of 128
@@ -70,12 +69,15 @@ cudaError_t launch_bwd_prep(const BwdPrepParams& p, int d, int dtype, cudaStream
 cudaError_t launch_bwd_dq(const BwdDqParams& p, int dtype, cudaStream_t stream);
 
 // Main kernel: grid = B * H_kv * n_kv_blocks CTAs of 384 threads.  Maps:
-// q, dO over [B*H, Nq, d]; k, v, dk, dv over [B*H_kv, Nkv, d].
+// q, dO over [B*H, Nq, d]; k, v, dk, dv over [B*H_kv, Nkv, d] (input dtype);
+// dq over the fp32 accumulator [B*H, Nq, d].
 cudaError_t launch_bwd_bf16(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                             const CUtensorMap& dout, const CUtensorMap& dk, const CUtensorMap& dv,
-                            const BwdParams& p, unsigned int grid, cudaStream_t stream);
+                            const CUtensorMap& dq, const BwdParams& p, unsigned int grid,
+                            cudaStream_t stream);
 cudaError_t launch_bwd_f16(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                            const CUtensorMap& dout, const CUtensorMap& dk, const CUtensorMap& dv,
-                           const BwdParams& p, unsigned int grid, cudaStream_t stream);
+                           const CUtensorMap& dq, const BwdParams& p, unsigned int grid,
+                           cudaStream_t stream);
 
 }  // namespace fa

@@ -31,8 +31,11 @@
 //   [256, 256 + d)  dV accumulator;  [256 + d, 256 + 2d)  dK accumulator.
 // Per query tile the issuer enqueues S^T, dP^T (after the previous dQ was
 // read out), dV += P^T dO, then dK += dS^T Q and dQ = dS K.  The gradient
-// warpgroups add the tile's dQ into an fp32 accumulator in global memory
-// with vector reductions; a last kernel scales and converts it.
+// warpgroups stage the tile's dQ (fp32) in the stage's Q and dO tiles, free
+// once dQ is computed, and add it into an fp32 accumulator in global memory
+// with TMA tensor reductions (whole 128-byte lines); the stage goes back to
+// the producer when both reductions have read it.  A last kernel scales and
+// converts the accumulator.
 //
 // Shared memory (128-byte-swizzled TMA tiles, 1024-byte aligned): K and V of
 // the key block (reused as the dK / dV output staging), a two-stage ring of
@@ -98,7 +101,7 @@ struct BwdCfg {
     // barrier slots
     static constexpr int kBarKV = 0;
     static constexpr int kBarFull = 1;                 // [kStages]
-    static constexpr int kBarEmpty = kBarFull + kStages;
+    static constexpr int kBarEmpty = kBarFull + kStages;  // both warpgroups' dQ reductions read the stage
     static constexpr int kBarS = kBarEmpty + kStages;  // S^T computed
     static constexpr int kBarDP = kBarS + 1;           // dP^T computed
     static constexpr int kBarP = kBarDP + 1;           // P^T in TMEM (8 warp arrivals)
@@ -156,11 +159,15 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
-// dst[0..3] += (a, b, c, d) in global memory (one 16-byte vector reduction).
-__device__ __forceinline__ void red_add_f32x4(float* dst, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c),
-                 "f"(d)
-                 : "memory");
+// 3-D tiled reduction shared -> global: the box at (c0, c1, c2) is added
+// element-wise (fp32) into the tensor; rows outside the tensor are skipped.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                                  int c2) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
 }
 
 __device__ __forceinline__ float bwd_u2f(uint32_t x) { return __uint_as_float(x); }
@@ -170,7 +177,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                   const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap map_dq, const BwdParams p) {
     using C = BwdCfg<D, F16>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -210,7 +217,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(C::kBarKV), 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar(C::kBarFull + s), 1);
-            mbar_init(bar(C::kBarEmpty + s), 1);
+            mbar_init(bar(C::kBarEmpty + s), 2);
         }
         mbar_init(bar(C::kBarS), 1);
         mbar_init(bar(C::kBarDP), 1);
@@ -231,6 +238,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_prefetch_desc(&map_k);
         tma_prefetch_desc(&map_v);
         tma_prefetch_desc(&map_do);
+        tma_prefetch_desc(&map_dq);
     }
     if (warp == kBwdMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), kBwdTmemCols);
@@ -350,7 +358,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mma_ss<false>(tDP, smem_desc_sw128(sDS + kk * C::kUmmaK * 128, C::kAtomBytes, 1024),
                                   mnmaj(sK, kk), C::kIdescDQ, kk > 0 ? 1u : 0u);
                 tc_commit(bar(C::kBarDQ));
-                tc_commit(bar(C::kBarEmpty + s));  // Q, dO and stats of stage s are no longer read
             }
             if (ok) tc_commit(bar(C::kBarAcc));
             // Drain every tensor-core operation before tensor memory is released.
@@ -459,29 +466,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::kBarDS));
 
-            // this tile's dQ (query row t, columns [w d/2, (w+1) d/2)) into the
-            // fp32 accumulator
+            // this tile's dQ (query row t, columns [w d/2, (w+1) d/2)): staged as
+            // fp32 boxes of 32 columns (128-byte swizzle) in the stage's Q tile
+            // (w = 0) or dO tile (w = 1), then added into the accumulator
             got = bwd_wait(bar(C::kBarDQ), it & 1, abort_flag, p, 43);
             ok = __all_sync(0xffffffffu, got);
             if (!ok) break;
             tc_fence_after();
-            const long long qrow = static_cast<long long>(qt) * 128 + t;
-            float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + static_cast<size_t>(qrow)) * D + w * (D / 2);
+            uint8_t* stg = smem + (w == 0 ? C::kOffQ : C::kOffDO) + s * C::kTileBytes;
 #pragma unroll
             for (int h = 0; h < D / 64; ++h) {
                 uint32_t v[32];
                 tmem_ld32(tDQ + 32u * h, v);
                 tmem_ld_wait(v);
-                if (qrow < p.Nq) {
+                uint8_t* rowp = stg + h * C::kAtomBytes + t * 128;
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        red_add_f32x4(dst + 32 * h + e, bwd_u2f(v[e]), bwd_u2f(v[e + 1]), bwd_u2f(v[e + 2]),
-                                      bwd_u2f(v[e + 3]));
-                }
+                for (int ch = 0; ch < 8; ++ch)
+                    *reinterpret_cast<uint4*>(rowp + ((ch ^ (t & 7)) << 4)) =
+                        make_uint4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
             }
             tc_fence_before();
+            fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::kBarDQFree));
+            named_barrier_sync(1 + w, 128);  // every row of this warpgroup's half is staged
+            if (t == 0) {
+#pragma unroll
+                for (int h = 0; h < D / 64; ++h)
+                    tma_reduce_add_3d(&map_dq, smem_u32(stg + h * C::kAtomBytes), w * (D / 2) + 32 * h, qt * 128, bh);
+                tma_store_commit();
+                tma_store_wait_read();
+                mbar_arrive(bar(C::kBarEmpty + s));
+            }
         }
 
         // ------------------------------------------------------- epilogue
@@ -546,7 +562,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 template <int D, bool F16, bool kCausal>
 cudaError_t launch_bwd_variant(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                const CUtensorMap& dout, const CUtensorMap& dk, const CUtensorMap& dv,
-                               const BwdParams& p, unsigned int grid, cudaStream_t stream) {
+                               const CUtensorMap& dq, const BwdParams& p, unsigned int grid,
+                               cudaStream_t stream) {
     using C = BwdCfg<D, F16>;
     auto kern = fa_bwd_kernel<D, F16, kCausal>;
     // The register split relies on the compiled kernel holding exactly
@@ -558,16 +575,16 @@ cudaError_t launch_bwd_variant(const CUtensorMap& q, const CUtensorMap& k, const
     if (attr.numRegs != static_cast<int>(kBwdLaunchRegs)) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemBytes));
     if (e != cudaSuccess) return e;
-    kern<<<grid, kBwdThreads, C::kSmemBytes, stream>>>(q, k, v, dout, dk, dv, p);
+    kern<<<grid, kBwdThreads, C::kSmemBytes, stream>>>(q, k, v, dout, dk, dv, dq, p);
     return cudaGetLastError();
 }
 
 template <int D, bool F16>
 cudaError_t launch_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                        const CUtensorMap& dout, const CUtensorMap& dk, const CUtensorMap& dv,
-                       const BwdParams& p, unsigned int grid, cudaStream_t stream) {
-    return p.causal ? launch_bwd_variant<D, F16, true>(q, k, v, dout, dk, dv, p, grid, stream)
-                    : launch_bwd_variant<D, F16, false>(q, k, v, dout, dk, dv, p, grid, stream);
+                       const CUtensorMap& dq, const BwdParams& p, unsigned int grid, cudaStream_t stream) {
+    return p.causal ? launch_bwd_variant<D, F16, true>(q, k, v, dout, dk, dv, dq, p, grid, stream)
+                    : launch_bwd_variant<D, F16, false>(q, k, v, dout, dk, dv, dq, p, grid, stream);
 }
 
 }  // namespace fa

@@ -141,6 +141,7 @@ class Workload:
     Nkv: int = 0           # key/value rows per head (0: N; N is the query rows)
     causal: bool = False   # query i sees keys j <= i + Nkv - N only
     splits: int = 1        # key-range partitions (0: as many as fill one wave)
+    backward: bool = False  # the step is the backward pass (dQ, dK, dV) for a fixed dO
     scale: np.float32 = field(init=False)
 
     def __post_init__(self):
@@ -169,14 +170,20 @@ class Workload:
         return float(np.clip(i + off + 1, 0, self.Nkv).sum())
 
     def flops(self) -> float:
-        """4 d flops per visible (query, key) pair: 4*B*H*N^2*d unmasked."""
-        return 4.0 * self.B * self.H * self.visible_pairs() * self.d
+        """Forward: 4 d flops per visible (query, key) pair (Q K^T and P V),
+        4*B*H*N^2*d unmasked.  Backward: 10 d per pair, the five products
+        K Q^T, V dO^T, P^T dO, dS^T Q and dS K (2.5x the forward)."""
+        per_pair = 10.0 if self.backward else 4.0
+        return per_pair * self.B * self.H * self.visible_pairs() * self.d
 
     def bytes(self) -> float:
-        """Algorithmic bytes: read q, k, v once, write o and lse."""
+        """Algorithmic bytes.  Forward: read q, k, v once, write o and lse.
+        Backward: read q, k, v, o, dO and lse once, write dq, dk, dv."""
         elem = 4 if self.dtype == "f32" else 2
-        return (elem * self.d * (2 * self.B * self.H * self.N + 2 * self.B * self.H_kv * self.Nkv)
-                + 4 * self.B * self.H * self.N)
+        q_rows, kv_rows = self.B * self.H * self.N, self.B * self.H_kv * self.Nkv
+        if self.backward:
+            return elem * self.d * (4 * q_rows + 4 * kv_rows) + 4 * q_rows
+        return elem * self.d * (2 * q_rows + 2 * kv_rows) + 4 * q_rows
 
     def describe(self) -> str:
         return f"{self.name}: B={self.B} H={self.H} N={self.N} d={self.d} {self.dtype}"
@@ -218,6 +225,19 @@ WORKLOADS["causal_b2h32_n8192_d128"] = Workload(
 WORKLOADS["f16_b2h32_n8192_d128"] = Workload(
     "f16_b2h32_n8192_d128", 2, 32, 8192, 128, "f16", seed=10, factor=0.5, oracle_rows=256,
     note="headline shape in fp16")
+# The backward pass (gradients for a seeded dO) on the headline shape, with
+# the causal mask, at d = 64, and on the half-size profiling case.
+WORKLOADS["bwd_b2h32_n8192_d128"] = Workload(
+    "bwd_b2h32_n8192_d128", 2, 32, 8192, 128, "bf16", seed=4, factor=0.5, backward=True,
+    note="backward pass on the headline shape, values x0.5")
+WORKLOADS["bwd_causal_b2h32_n8192_d128"] = Workload(
+    "bwd_causal_b2h32_n8192_d128", 2, 32, 8192, 128, "bf16", seed=9, factor=0.5, causal=True,
+    backward=True, note="backward pass, causal mask")
+WORKLOADS["bwd_b4h16_n2048"] = Workload(
+    "bwd_b4h16_n2048", 4, 16, 2048, 64, "bf16", seed=3, backward=True, note="backward pass, d = 64")
+WORKLOADS["bwd_b1h32_n8192_d128"] = Workload(
+    "bwd_b1h32_n8192_d128", 1, 32, 8192, 128, "bf16", seed=6, factor=0.5, backward=True,
+    note="backward profiling case: half the headline shape")
 HEADLINE = "b2h32_n8192_d128"
 SMALL = "single_head_n512"
 
