@@ -20,11 +20,11 @@ constexpr size_t kWsAlign = 256;
 
 int64_t pad128(int64_t n) { return (n + 127) / 128 * 128; }
 
-// Workspace: [row statistics: B*H*Nq_pad RowStat, padded to 256 bytes]
+// Workspace: [row statistics: 2 floats per padded query row, padded to 256 bytes]
 //            [dQ accumulator: B*H*Nq*d fp32]
 size_t stats_bytes(int64_t B, int64_t H, int64_t N_q) {
     const size_t n = static_cast<size_t>(B) * static_cast<size_t>(H) * static_cast<size_t>(pad128(N_q)) *
-                     sizeof(fa::RowStat);
+                     2 * sizeof(float);
     return (n + kWsAlign - 1) / kWsAlign * kWsAlign;
 }
 size_t workspace_bytes(int64_t B, int64_t H, int64_t N_q, int64_t d) {
@@ -97,7 +97,7 @@ int launch_bwd_all(const void* q, const void* k, const void* v, const void* o, c
     if ((st = encode_map(&mdv, dv, dtype, BHkv, N_kv, d)) != FA_OK) return st;
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    fa::RowStat* stats = reinterpret_cast<fa::RowStat*>(ws);
+    float* stats = reinterpret_cast<float*>(ws);
     float* dq_acc = reinterpret_cast<float*>(ws + stats_bytes(B, H, N_q));
     if ((st = encode_map(&mdq, dq_acc, FA_DTYPE_F32, BH, N_q, d)) != FA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -22,8 +22,13 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdPrepParams p)
     if (row >= p.rows_pad) return;
     const long long bh = row / p.Nq_pad;
     const int i = static_cast<int>(row % p.Nq_pad);
+    // rows of a tile are consecutive (Nq_pad is a multiple of 128)
+    float* st = p.stats + (row / 128) * kStatFloatsPerTile + (row % 128);
     if (i >= p.Nq) {  // padding row of the last query tile: weight 0, no gradient
-        if (lane == 0) p.stats[row] = RowStat{-INFINITY, 0.0f};
+        if (lane == 0) {
+            st[0] = -INFINITY;
+            st[128] = 0.0f;
+        }
         return;
     }
     const size_t r = static_cast<size_t>(bh) * static_cast<size_t>(p.Nq) + static_cast<size_t>(i);
@@ -50,8 +55,8 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const BwdPrepParams p)
     if (lane == 0) {
         const float lse = p.lse[r];
         // a row with no visible key (lse = -inf) gets weight 0 everywhere
-        const float nlse2 = (lse == -INFINITY) ? -INFINITY : -lse * 1.4426950408889634f;
-        p.stats[row] = RowStat{nlse2, acc};
+        st[0] = (lse == -INFINITY) ? -INFINITY : -lse * 1.4426950408889634f;
+        st[128] = acc;
     }
 }
 

@@ -20,18 +20,18 @@
 
 namespace fa {
 
-// Row statistics of one query row, as the main kernel reads them.
-struct RowStat {
-    float nlse2;  // -lse * log2(e), or -inf for a padding row or a row with no visible key
-    float D;      // sum_c dO[c] * O[c]; 0 for a padding row
-};
+// Row statistics, one 1 KB block per 128-row query tile (tile t of head bh
+// is block bh * Nq_pad / 128 + t): 128 floats -lse * log2(e) (-inf for a
+// padding row or a row with no visible key), then 128 floats
+// D = sum_c dO[c] * O[c] (0 for a padding row).
+constexpr int kStatFloatsPerTile = 256;
 
 // Parameters of the prep kernel.
 struct BwdPrepParams {
     const void* o;        // [B*H, Nq, d] input dtype
     const void* dout;     // [B*H, Nq, d] input dtype
     const float* lse;     // [B*H, Nq] natural log
-    RowStat* stats;       // [B*H, Nq_pad]
+    float* stats;         // B*H*Nq_pad/128 blocks of kStatFloatsPerTile
     float* dq_acc;        // [B*H, Nq, d] fp32, zeroed here
     long long rows_pad;   // B*H*Nq_pad
     int Nq;
@@ -42,7 +42,7 @@ struct BwdPrepParams {
 struct BwdParams {
     DevStatus* status;    // device status word of the current device
     unsigned int gen;     // this launch's generation (never 0)
-    const RowStat* stats; // [B*H, Nq_pad]
+    const float* stats;   // B*H*Nq_pad/128 blocks of kStatFloatsPerTile
     int Nq;               // query rows per head
     int Nkv;              // key / value rows per head
     int Nq_pad;           // Nq rounded up to a multiple of 128

@@ -23,19 +23,23 @@
 // from tensor memory.
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
-//   [0, 128)        S^T = K Q^T of the current tile.  Warpgroup w then
-//                   writes P^T (bf16/fp16 pairs) over its columns
-//                   [64w, 64w + 32) and dS^T over [64w + 32, 64w + 64).
-//   [128, 256)      dP^T = V dO^T; once dS is formed, the tile's dQ = dS K
-//                   (query rows on the lanes, d columns).
+//   [0, 128)        S^T = K Q^T of the current tile; warpgroup w then writes
+//                   P^T (bf16/fp16 pairs) over its columns [64w, 64w + 32).
+//   [128, 256)      dP^T = V dO^T; warpgroup w then writes dS^T over
+//                   [128 + 64w, 128 + 64w + 32).
 //   [256, 256 + d)  dV accumulator;  [256 + d, 256 + 2d)  dK accumulator.
-// Per query tile the issuer enqueues S^T, dP^T (after the previous dQ was
-// read out), dV += P^T dO, then dK += dS^T Q and dQ = dS K.  The gradient
-// warpgroups stage the tile's dQ (fp32) in the stage's Q and dO tiles, free
-// once dQ is computed, and add it into an fp32 accumulator in global memory
-// with TMA tensor reductions (whole 128-byte lines); the stage goes back to
-// the producer when both reductions have read it.  A last kernel scales and
-// converts the accumulator.
+//   dQ = dS K of a tile (query rows on the lanes, d columns): columns
+//   [384, 448) for d = 64; for d = 128 over the dP^T columns, so the next
+//   tile's dP^T waits until this dQ has been read out.
+// Per query tile j the issuer enqueues dP^T(j), dV(j) += P^T dO once P^T(j)
+// is written, S^T(j+1) (over P^T(j), which dV(j) has consumed: one issuing
+// thread, executed in order), then dK(j) += dS^T Q and dQ(j) = dS K once
+// dS(j) is written.  The gradient warpgroups form dS(j), then P^T(j+1) while
+// dK(j) and dQ(j) run, then read dQ(j) out: staged (fp32) in the stage's Q
+// and dO tiles, free once dQ(j) is computed, and added into an fp32
+// accumulator in global memory with TMA tensor reductions (whole 128-byte
+// lines); the stage goes back to the producer when both reductions have read
+// it.  A last kernel scales and converts the accumulator.
 //
 // Shared memory (128-byte-swizzled TMA tiles, 1024-byte aligned): K and V of
 // the key block (reused as the dK / dV output staging), a two-stage ring of
@@ -59,10 +63,11 @@ namespace fa {
 constexpr int kBwdThreads = 384;
 constexpr int kBwdMmaWarp = 8;
 constexpr int kBwdLoadWarp = 9;
+constexpr int kBwdReduceWarp = 10;
 constexpr uint32_t kBwdLaunchRegs = 168;
 constexpr uint32_t kBwdTmemCols = 512;
 constexpr uint64_t kBwdWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
-constexpr int kBwdStatBytes = 128 * static_cast<int>(sizeof(RowStat));  // one query tile
+constexpr int kBwdStatBytes = kStatFloatsPerTile * static_cast<int>(sizeof(float));  // one query tile
 
 template <int D, bool F16>
 struct BwdCfg {
@@ -101,7 +106,7 @@ struct BwdCfg {
     // barrier slots
     static constexpr int kBarKV = 0;
     static constexpr int kBarFull = 1;                 // [kStages]
-    static constexpr int kBarEmpty = kBarFull + kStages;  // both warpgroups' dQ reductions read the stage
+    static constexpr int kBarEmpty = kBarFull + kStages;  // the stage's dQ reductions have read it
     static constexpr int kBarS = kBarEmpty + kStages;  // S^T computed
     static constexpr int kBarDP = kBarS + 1;           // dP^T computed
     static constexpr int kBarP = kBarDP + 1;           // P^T in TMEM (8 warp arrivals)
@@ -111,7 +116,8 @@ struct BwdCfg {
     static constexpr int kBarAcc = kBarDQFree + 1;     // dK, dV final
     static constexpr int kBarDrain = kBarAcc + 1;
     static constexpr int kBarEpi = kBarDrain + 1;      // [2]
-    static constexpr int kNumBars = kBarEpi + 2;
+    static constexpr int kBarStaged = kBarEpi + 2;     // [kStages]: the tile's dQ is staged (8)
+    static constexpr int kNumBars = kBarStaged + kStages;
     // barriers, TMEM slot and abort flag
     static constexpr int kCtrlBytes = kNumBars * 8 + 8;
     // The control block lives in whichever alignment gap holds it: below the
@@ -121,6 +127,23 @@ struct BwdCfg {
     static_assert(kCtrlBytes <= 512, "control block must fit either gap");
     static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
     static_assert(256 + 2 * D <= static_cast<int>(kBwdTmemCols), "tensor memory budget exceeded");
+
+    // tensor-memory columns
+    static constexpr uint32_t kColS = 0;      // S^T; P^T of warpgroup w at [64w, 64w + 32)
+    static constexpr uint32_t kColDP = 128;   // dP^T; dS^T of warpgroup w at [128 + 64w, 128 + 64w + 32)
+    static constexpr uint32_t kColDV = 256;
+    static constexpr uint32_t kColDK = 256 + D;
+    // dQ of a tile: its own columns when they fit (d = 64), else over the dP
+    // columns (d = 128), which the next tile's dP^T may then only overwrite
+    // once dQ has been read out
+    static constexpr bool kDqOwnCols = 256 + 3 * D <= static_cast<int>(kBwdTmemCols);
+    static constexpr uint32_t kColDQ = kDqOwnCols ? 256 + 2 * D : 128;
+    // Issue order.  With dQ in its own columns, S^T(j+1) goes right after
+    // dV(j) and the gradient warpgroups form P^T(j+1) while dK(j) and dQ(j)
+    // run.  With dQ over the dP^T columns, dP^T(j+1) must wait for the
+    // read-out of dQ(j) anyway: S^T(j+1) then follows dQ(j) and runs during
+    // that read-out, and P^T(j+1) comes after it.
+    static constexpr bool kEarlyS = kDqOwnCols;
 };
 
 // Bounded wait on an mbarrier phase (the forward kernel's policy): returns
@@ -217,7 +240,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(C::kBarKV), 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar(C::kBarFull + s), 1);
-            mbar_init(bar(C::kBarEmpty + s), 2);
+            mbar_init(bar(C::kBarEmpty + s), 1);
+            mbar_init(bar(C::kBarStaged + s), 8);
         }
         mbar_init(bar(C::kBarS), 1);
         mbar_init(bar(C::kBarDP), 1);
@@ -283,7 +307,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                 bar(C::kBarFull + s), a * C::kAtomElems, qt * 128, bh, keep);
                 }
                 bulk_load(sbase + C::kOffStats + s * kBwdStatBytes,
-                          p.stats + static_cast<size_t>(bh) * p.Nq_pad + static_cast<size_t>(qt) * 128,
+                          p.stats + (static_cast<size_t>(bh) * (p.Nq_pad / 128) + static_cast<size_t>(qt)) *
+                                        kStatFloatsPerTile,
                           kBwdStatBytes, bar(C::kBarFull + s), keep);
                 issued = it + 1;
             }
@@ -294,13 +319,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 bwd_wait(bar(C::kBarFull + s), (last / C::kStages) & 1, abort_flag, p, 32, false);
             }
         }
+      } else if (warp == kBwdReduceWarp) {
+        // ------------------------------------------------------ dQ reducer
+        // Adds each tile's staged dQ (warpgroup 0's columns in the stage's Q
+        // tile, warpgroup 1's in its dO tile) into the fp32 accumulator and
+        // hands the stage back to the producer once the reductions have read
+        // it.  The gradient warpgroups never wait for the L2.
+        if (lane == 0) {
+            for (int it = 0; it < T; ++it) {
+                const int s = it % C::kStages;
+                if (!bwd_wait(bar(C::kBarStaged + s), (it / C::kStages) & 1, abort_flag, p, 39)) break;
+                const int qt = qt_begin + it % nqt;
+                const int bh = b * p.H + kvh * p.group + it / nqt;
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    const uint32_t stg = sbase + (w == 0 ? C::kOffQ : C::kOffDO) + s * C::kTileBytes;
+#pragma unroll
+                    for (int h = 0; h < D / 64; ++h)
+                        tma_reduce_add_3d(&map_dq, stg + h * C::kAtomBytes, w * (D / 2) + 32 * h, qt * 128, bh);
+                }
+                tma_store_commit();
+                tma_store_wait_read();
+                mbar_arrive(bar(C::kBarEmpty + s));
+            }
+        }
       } else if (warp == kBwdMmaWarp) {
         // ------------------------------------------------ tensor-core issuer
+        // Order per tile j: dP^T(j), dV(j) once P^T(j) is written, S^T(j+1)
+        // right after (it overwrites P^T(j), which dV(j) has consumed: same
+        // thread, the tensor core runs them in order), then dK(j) and dQ(j)
+        // once dS(j) is written.  The gradient warpgroups compute P^T(j+1)
+        // while dK(j) and dQ(j) run.
         if (lane == 0) {
-            const uint32_t tS = tmem;             // S^T, then P^T / dS^T
-            const uint32_t tDP = tmem + 128u;     // dP^T, then dQ
-            const uint32_t tDV = tmem + 256u;
-            const uint32_t tDK = tmem + 256u + static_cast<uint32_t>(D);
+            const uint32_t tS = tmem + C::kColS;
+            const uint32_t tDP = tmem + C::kColDP;
+            const uint32_t tDV = tmem + C::kColDV;
+            const uint32_t tDK = tmem + C::kColDK;
+            const uint32_t tDQ = tmem + C::kColDQ;
             const uint32_t sK = sbase + C::kOffK;
             const uint32_t sV = sbase + C::kOffV;
             const uint32_t sDS = sbase + C::kOffDS;
@@ -314,21 +369,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             auto mnmaj = [&](uint32_t tile, int kk) {
                 return smem_desc_sw128(tile + kk * C::kUmmaK * 128, C::kAtomBytes, 1024);
             };
-            bool ok = bwd_wait(bar(C::kBarKV), 0, abort_flag, p, 33);
-            for (int it = 0; ok && it < T; ++it) {
-                const int s = it % C::kStages;
-                ok = bwd_wait(bar(C::kBarFull + s), (it / C::kStages) & 1, abort_flag, p, 34);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t sQ = sbase + C::kOffQ + s * C::kTileBytes;
-                const uint32_t sDO = sbase + C::kOffDO + s * C::kTileBytes;
-                // S^T = K Q^T
+            auto stage_q = [&](int j) { return sbase + C::kOffQ + (j % C::kStages) * C::kTileBytes; };
+            auto stage_do = [&](int j) { return sbase + C::kOffDO + (j % C::kStages) * C::kTileBytes; };
+            // S^T(j) = K Q_j^T
+            auto issue_s = [&](int j) {
 #pragma unroll
                 for (int kk = 0; kk < C::kDSteps; ++kk)
-                    mma_ss<false>(tS, kmaj(sK, kk), kmaj(sQ, kk), C::kIdescS, kk > 0 ? 1u : 0u);
+                    mma_ss<false>(tS, kmaj(sK, kk), kmaj(stage_q(j), kk), C::kIdescS, kk > 0 ? 1u : 0u);
                 tc_commit(bar(C::kBarS));
-                // dP^T = V dO^T, into the columns the previous tile's dQ occupied
-                if (it > 0) {
+            };
+
+            bool ok = bwd_wait(bar(C::kBarKV), 0, abort_flag, p, 33);
+            if (ok) ok = bwd_wait(bar(C::kBarFull + 0), 0, abort_flag, p, 34);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+            }
+            for (int it = 0; ok && it < T; ++it) {
+                const uint32_t sQ = stage_q(it);
+                const uint32_t sDO = stage_do(it);
+                // dP^T = V dO^T (d = 128: into the columns the previous dQ occupied)
+                if (!C::kDqOwnCols && it > 0) {
                     ok = bwd_wait(bar(C::kBarDQFree), (it - 1) & 1, abort_flag, p, 35);
                     if (!ok) break;
                     tc_fence_after();
@@ -345,19 +406,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 for (int kk = 0; kk < C::kRowSteps; ++kk)
                     mma_ts<false>(tDV, tS + (kk / 4) * 64 + (kk % 4) * 8, mnmaj(sDO, kk), C::kIdescAcc,
                                   (it > 0 || kk > 0) ? 1u : 0u);
-                // dK += dS^T Q, then this tile's dQ = dS K
+                // the next tile's scores (early order)
+                if (C::kEarlyS && it + 1 < T) {
+                    ok = bwd_wait(bar(C::kBarFull + (it + 1) % C::kStages), ((it + 1) / C::kStages) & 1,
+                                  abort_flag, p, 34);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(it + 1);
+                }
+                // dK += dS^T Q (dS^T read K-major from the dS tile), then this
+                // tile's dQ = dS K (the same tile read MN-major)
                 ok = bwd_wait(bar(C::kBarDS), it & 1, abort_flag, p, 37);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < C::kRowSteps; ++kk)
-                    mma_ts<false>(tDK, tS + (kk / 4) * 64 + 32 + (kk % 4) * 8, mnmaj(sQ, kk), C::kIdescAcc,
-                                  (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_ss<false>(tDK, kmaj(sDS, kk), mnmaj(sQ, kk), C::kIdescAcc, (it > 0 || kk > 0) ? 1u : 0u);
+                if (C::kDqOwnCols && it > 0) {  // the previous dQ has been read out
+                    ok = bwd_wait(bar(C::kBarDQFree), (it - 1) & 1, abort_flag, p, 35);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
 #pragma unroll
                 for (int kk = 0; kk < C::kRowSteps; ++kk)
-                    mma_ss<false>(tDP, smem_desc_sw128(sDS + kk * C::kUmmaK * 128, C::kAtomBytes, 1024),
+                    mma_ss<false>(tDQ, smem_desc_sw128(sDS + kk * C::kUmmaK * 128, C::kAtomBytes, 1024),
                                   mnmaj(sK, kk), C::kIdescDQ, kk > 0 ? 1u : 0u);
                 tc_commit(bar(C::kBarDQ));
+                // the next tile's scores (late order: they run during dQ's read-out)
+                if (!C::kEarlyS && it + 1 < T) {
+                    ok = bwd_wait(bar(C::kBarFull + (it + 1) % C::kStages), ((it + 1) / C::kStages) & 1,
+                                  abort_flag, p, 34);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(it + 1);
+                }
             }
             if (ok) tc_commit(bar(C::kBarAcc));
             // Drain every tensor-core operation before tensor memory is released.
@@ -367,79 +449,95 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     } else {
         // ----------------------------------------------- gradient warpgroups
+        // Order per tile j: dS(j) once dP^T(j) is ready, then P^T(j+1) (its
+        // scores were issued right after dV(j)), then the read-out of dQ(j).
         regs_increase<C::kGradRegs>();
         const int w = warp / 4;         // query columns [64w, 64w + 64) of each tile
         const int wi = warp % 4;        // TMEM lane quarter this warp may access
         const int t = wi * 32 + lane;   // key row of the block (= TMEM lane); query row for dQ
         const uint32_t lane_off = static_cast<uint32_t>(wi * 32) << 16;
-        const uint32_t tS = tmem + lane_off + 64u * static_cast<uint32_t>(w);
-        const uint32_t tDP = tmem + lane_off + 128u + 64u * static_cast<uint32_t>(w);
-        const uint32_t tDQ = tmem + lane_off + 128u + static_cast<uint32_t>(w * (D / 2));
+        const uint32_t tS = tmem + lane_off + C::kColS + 64u * static_cast<uint32_t>(w);
+        const uint32_t tDP = tmem + lane_off + C::kColDP + 64u * static_cast<uint32_t>(w);
+        const uint32_t tDQ = tmem + lane_off + C::kColDQ + static_cast<uint32_t>(w * (D / 2));
         const long long key = static_cast<long long>(kb) * 128 + t;
         const bool key_valid = key < p.Nkv;  // rows past Nkv were zero-filled: weight 0
         const float c = p.scale_log2;
         bool ok = true;
+        uint32_t x[2][32];  // P^T of the current tile in fp32: this key, 64 query columns
 
-        for (int it = 0; it < T; ++it) {
-            const int s = it % C::kStages;
-            const int qt = qt_begin + it % nqt;
-            const int bh = b * p.H + kvh * p.group + it / nqt;
-            // the stage's statistics have landed, and S^T is ready
-            bool got = bwd_wait(bar(C::kBarFull + s), (it / C::kStages) & 1, abort_flag, p, 40);
-            if (got) got = bwd_wait(bar(C::kBarS), it & 1, abort_flag, p, 41);
-            ok = __all_sync(0xffffffffu, got);
-            if (!ok) break;
+        // P^T(j) = 2^(S^T scale log2(e) - lse_i log2(e)) into x and, as 16-bit
+        // pairs, over this warpgroup's first 32 S^T columns
+        auto p_phase = [&](int j) -> bool {
+            const int sj = j % C::kStages;
+            const int qt = qt_begin + j % nqt;
+            // the stage's statistics have landed, and S^T(j) is ready
+            bool got = bwd_wait(bar(C::kBarFull + sj), (j / C::kStages) & 1, abort_flag, p, 40);
+            if (got) got = bwd_wait(bar(C::kBarS), j & 1, abort_flag, p, 41);
+            if (!__all_sync(0xffffffffu, got)) return false;
             tc_fence_after();
-
-            uint32_t x[2][32];
             tmem_ld32(tS, x[0]);
             tmem_ld32(tS + 32u, x[1]);
             tmem_ld_wait(x[0]);
             tmem_ld_wait(x[1]);
-            // statistics of query columns 64w + 2m, 64w + 2m + 1: {nlse2, D, nlse2, D}
-            const float4* st4 = reinterpret_cast<const float4*>(smem + C::kOffStats + s * kBwdStatBytes) + 32 * w;
+            // -lse log2(e) of this warpgroup's 64 query columns
+            const float4* nl4 = reinterpret_cast<const float4*>(smem + C::kOffStats + sj * kBwdStatBytes) + 16 * w;
             // causal: query column q (index qt*128 + q) sees this key iff q >= thr
             int thr = 0;
             if (kCausal) {
                 const long long v = key - p.causal_offset - static_cast<long long>(qt) * 128;
                 thr = static_cast<int>(v < -1 ? -1 : (v > 129 ? 129 : v));
             }
-
-            // P^T = 2^(S^T scale log2(e) - lse_i log2(e)), kept in fp32 in x and
-            // written as 16-bit pairs over this warpgroup's first 32 columns
-            uint32_t pk[32];
+            const uint64_t c2 = f2_pack(c, c);
+            uint32_t pk[32];  // pair m: query columns 64w + 2m, 64w + 2m + 1
 #pragma unroll
-            for (int m = 0; m < 32; ++m) {
-                const float4 st = st4[m];
-                const int h = m / 16, e = (m % 16) * 2;
-                float p0 = ex2(fmaf(bwd_u2f(x[h][e]), c, st.x));
-                float p1 = ex2(fmaf(bwd_u2f(x[h][e + 1]), c, st.z));
-                if (kCausal) {
-                    const int q0 = 64 * w + 2 * m;
-                    if (q0 < thr) p0 = 0.0f;
-                    if (q0 + 1 < thr) p1 = 0.0f;
+            for (int m4 = 0; m4 < 16; ++m4) {
+                const float4 nl = nl4[m4];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int m = 2 * m4 + hh, h = m / 16, e = (m % 16) * 2;
+                    float t0, t1;
+                    f2_unpack(f2_fma(f2_pack(bwd_u2f(x[h][e]), bwd_u2f(x[h][e + 1])), c2,
+                                     hh == 0 ? f2_pack(nl.x, nl.y) : f2_pack(nl.z, nl.w)),
+                              t0, t1);
+                    float p0 = ex2(t0), p1 = ex2(t1);
+                    if (kCausal) {
+                        const int q0 = 64 * w + 2 * m;
+                        if (q0 < thr) p0 = 0.0f;
+                        if (q0 + 1 < thr) p1 = 0.0f;
+                    }
+                    if (!key_valid) {
+                        p0 = 0.0f;
+                        p1 = 0.0f;
+                    }
+                    x[h][e] = __float_as_uint(p0);
+                    x[h][e + 1] = __float_as_uint(p1);
+                    pk[m] = pack_16x2<F16>(p0, p1);
                 }
-                if (!key_valid) {
-                    p0 = 0.0f;
-                    p1 = 0.0f;
-                }
-                x[h][e] = __float_as_uint(p0);
-                x[h][e + 1] = __float_as_uint(p1);
-                pk[m] = pack_16x2<F16>(p0, p1);
             }
             tmem_st32(tS, pk);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::kBarP));
+            return true;
+        };
 
-            got = bwd_wait(bar(C::kBarDP), it & 1, abort_flag, p, 42);
+        if (T > 0) ok = p_phase(0);
+        for (int it = 0; ok && it < T; ++it) {
+            const int s = it % C::kStages;
+            const int qt = qt_begin + it % nqt;
+            const int bh = b * p.H + kvh * p.group + it / nqt;
+
+            // dS^T = P^T o (dP^T - D), as 16-bit pairs into row t of atom w of
+            // the dS tile (free: the previous dK and dQ have completed)
+            bool got = bwd_wait(bar(C::kBarDP), it & 1, abort_flag, p, 42);
             ok = __all_sync(0xffffffffu, got);
             if (!ok) break;
             tc_fence_after();
-            // dS^T = P^T o (dP^T - D), written as 16-bit pairs over the next 32
-            // columns and, for dQ = dS K, into row t of shared-memory atom w
-            uint32_t dpk[32];
+            const float4* d4 =
+                reinterpret_cast<const float4*>(smem + C::kOffStats + s * kBwdStatBytes + kBwdStatBytes / 2) + 16 * w;
+            const float* dcol = reinterpret_cast<const float*>(d4);
+            uint32_t dpk[32];  // pair m: query columns 64w + 2m, 64w + 2m + 1
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t dp[32];
@@ -448,55 +546,60 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     const int m = h * 16 + e / 2;
-                    const float4 st = st4[m];
-                    const float d0 = bwd_u2f(x[h][e]) * (bwd_u2f(dp[e]) - st.y);
-                    const float d1 = bwd_u2f(x[h][e + 1]) * (bwd_u2f(dp[e + 1]) - st.w);
+                    const float d0 = bwd_u2f(x[h][e]) * (bwd_u2f(dp[e]) - dcol[2 * m]);
+                    const float d1 = bwd_u2f(x[h][e + 1]) * (bwd_u2f(dp[e + 1]) - dcol[2 * m + 1]);
                     dpk[m] = pack_16x2<F16>(d0, d1);
                 }
             }
-            tmem_st32(tS + 32u, dpk);
             uint8_t* row_ptr = smem + C::kOffDS + w * C::kAtomBytes + t * 128;
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
                 *reinterpret_cast<uint4*>(row_ptr + ((ch ^ (t & 7)) << 4)) =
                     make_uint4(dpk[4 * ch], dpk[4 * ch + 1], dpk[4 * ch + 2], dpk[4 * ch + 3]);
             fence_proxy_async_smem();
-            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::kBarDS));
 
+            // the next tile's P^T while dK and dQ of this tile run (early order)
+            if (C::kEarlyS && it + 1 < T) {
+                ok = p_phase(it + 1);
+                if (!ok) break;
+            }
+
             // this tile's dQ (query row t, columns [w d/2, (w+1) d/2)): staged as
             // fp32 boxes of 32 columns (128-byte swizzle) in the stage's Q tile
-            // (w = 0) or dO tile (w = 1), then added into the accumulator
+            // (w = 0) or dO tile (w = 1), which the reducer adds into the
+            // accumulator
             got = bwd_wait(bar(C::kBarDQ), it & 1, abort_flag, p, 43);
             ok = __all_sync(0xffffffffu, got);
             if (!ok) break;
             tc_fence_after();
             uint8_t* stg = smem + (w == 0 ? C::kOffQ : C::kOffDO) + s * C::kTileBytes;
+            uint32_t v[D / 64][32];
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h) tmem_ld32(tDQ + 32u * h, v[h]);
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h) tmem_ld_wait(v[h]);
 #pragma unroll
             for (int h = 0; h < D / 64; ++h) {
-                uint32_t v[32];
-                tmem_ld32(tDQ + 32u * h, v);
-                tmem_ld_wait(v);
                 uint8_t* rowp = stg + h * C::kAtomBytes + t * 128;
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch)
                     *reinterpret_cast<uint4*>(rowp + ((ch ^ (t & 7)) << 4)) =
-                        make_uint4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
+                        make_uint4(v[h][4 * ch], v[h][4 * ch + 1], v[h][4 * ch + 2], v[h][4 * ch + 3]);
             }
             tc_fence_before();
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::kBarDQFree));
-            named_barrier_sync(1 + w, 128);  // every row of this warpgroup's half is staged
-            if (t == 0) {
-#pragma unroll
-                for (int h = 0; h < D / 64; ++h)
-                    tma_reduce_add_3d(&map_dq, smem_u32(stg + h * C::kAtomBytes), w * (D / 2) + 32 * h, qt * 128, bh);
-                tma_store_commit();
-                tma_store_wait_read();
-                mbar_arrive(bar(C::kBarEmpty + s));
+            if (lane == 0) {
+                mbar_arrive(bar(C::kBarDQFree));    // its tensor-memory columns are free
+                mbar_arrive(bar(C::kBarStaged + s));  // the reducer may read the staged rows
+            }
+            // the next tile's P^T (late order)
+            if (!C::kEarlyS && it + 1 < T) {
+                ok = p_phase(it + 1);
+                if (!ok) break;
             }
         }
 
