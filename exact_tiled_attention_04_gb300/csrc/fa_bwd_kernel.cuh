@@ -105,9 +105,14 @@ struct BwdCfg {
 
     // barrier slots
     static constexpr int kBarKV = 0;
-    static constexpr int kBarFull = 1;                 // [kStages]
-    static constexpr int kBarEmpty = kBarFull + kStages;  // the stage's dQ reductions have read it
-    static constexpr int kBarS = kBarEmpty + kStages;  // S^T computed
+    // A stage is two halves with their own barriers: Q with the row
+    // statistics, and dO.  Each half is handed back as soon as the dQ
+    // reduction staged in it has read it.
+    static constexpr int kBarFull = 1;                      // [kStages] Q + statistics landed
+    static constexpr int kBarFullDO = kBarFull + kStages;   // [kStages] dO landed
+    static constexpr int kBarEmpty = kBarFullDO + kStages;  // [kStages] Q half free
+    static constexpr int kBarEmptyDO = kBarEmpty + kStages; // [kStages] dO half free
+    static constexpr int kBarS = kBarEmptyDO + kStages;     // S^T computed
     static constexpr int kBarDP = kBarS + 1;           // dP^T computed
     static constexpr int kBarP = kBarDP + 1;           // P^T in TMEM (8 warp arrivals)
     static constexpr int kBarDS = kBarP + 1;           // dS^T in TMEM and dS in smem (8)
@@ -193,6 +198,12 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32
         : "memory");
 }
 
+// Wait until at most N committed bulk groups of this thread still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ float bwd_u2f(uint32_t x) { return __uint_as_float(x); }
 
 template <int D, bool F16, bool kCausal>
@@ -240,7 +251,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(bar(C::kBarKV), 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar(C::kBarFull + s), 1);
+            mbar_init(bar(C::kBarFullDO + s), 1);
             mbar_init(bar(C::kBarEmpty + s), 1);
+            mbar_init(bar(C::kBarEmptyDO + s), 1);
             mbar_init(bar(C::kBarStaged + s), 8);
         }
         mbar_init(bar(C::kBarS), 1);
@@ -292,31 +305,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tma_load_3d(sbase + C::kOffV + a * C::kAtomBytes, &map_v, bar(C::kBarKV), a * C::kAtomElems,
                             kb * 128, unit, once);
             }
-            int issued = 0;
+            int issued_q = 0, issued_do = 0;
             for (int it = 0; it < T; ++it) {
                 const int s = it % C::kStages;
-                if (!bwd_wait(bar(C::kBarEmpty + s), ((it / C::kStages) & 1) ^ 1, abort_flag, p, 31)) break;
+                const uint32_t ph = ((it / C::kStages) & 1) ^ 1;
                 const int g = it / nqt;
                 const int qt = qt_begin + it % nqt;
                 const int bh = b * p.H + kvh * p.group + g;
-                mbar_arrive_expect_tx(bar(C::kBarFull + s), 2u * C::kTileBytes + kBwdStatBytes);
-                for (int a = 0; a < C::kAtoms; ++a) {
+                if (!bwd_wait(bar(C::kBarEmpty + s), ph, abort_flag, p, 31)) break;
+                mbar_arrive_expect_tx(bar(C::kBarFull + s), C::kTileBytes + kBwdStatBytes);
+                for (int a = 0; a < C::kAtoms; ++a)
                     tma_load_3d(sbase + C::kOffQ + s * C::kTileBytes + a * C::kAtomBytes, &map_q,
                                 bar(C::kBarFull + s), a * C::kAtomElems, qt * 128, bh, keep);
-                    tma_load_3d(sbase + C::kOffDO + s * C::kTileBytes + a * C::kAtomBytes, &map_do,
-                                bar(C::kBarFull + s), a * C::kAtomElems, qt * 128, bh, keep);
-                }
                 bulk_load(sbase + C::kOffStats + s * kBwdStatBytes,
                           p.stats + (static_cast<size_t>(bh) * (p.Nq_pad / 128) + static_cast<size_t>(qt)) *
                                         kStatFloatsPerTile,
                           kBwdStatBytes, bar(C::kBarFull + s), keep);
-                issued = it + 1;
+                issued_q = it + 1;
+                if (!bwd_wait(bar(C::kBarEmptyDO + s), ph, abort_flag, p, 31)) break;
+                mbar_arrive_expect_tx(bar(C::kBarFullDO + s), C::kTileBytes);
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_3d(sbase + C::kOffDO + s * C::kTileBytes + a * C::kAtomBytes, &map_do,
+                                bar(C::kBarFullDO + s), a * C::kAtomElems, qt * 128, bh, keep);
+                issued_do = it + 1;
             }
             // Drain: every issued load has landed before the CTA may exit.
             bwd_wait(bar(C::kBarKV), 0, abort_flag, p, 32, false);
-            for (int s = 0; s < C::kStages && s < issued; ++s) {
-                const int last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
-                bwd_wait(bar(C::kBarFull + s), (last / C::kStages) & 1, abort_flag, p, 32, false);
+            for (int s = 0; s < C::kStages; ++s) {
+                if (s < issued_q) {
+                    const int last = s + ((issued_q - 1 - s) / C::kStages) * C::kStages;
+                    bwd_wait(bar(C::kBarFull + s), (last / C::kStages) & 1, abort_flag, p, 32, false);
+                }
+                if (s < issued_do) {
+                    const int last = s + ((issued_do - 1 - s) / C::kStages) * C::kStages;
+                    bwd_wait(bar(C::kBarFullDO + s), (last / C::kStages) & 1, abort_flag, p, 32, false);
+                }
             }
         }
       } else if (warp == kBwdReduceWarp) {
@@ -337,10 +360,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                     for (int h = 0; h < D / 64; ++h)
                         tma_reduce_add_3d(&map_dq, stg + h * C::kAtomBytes, w * (D / 2) + 32 * h, qt * 128, bh);
+                    tma_store_commit();  // one group per half
                 }
-                tma_store_commit();
-                tma_store_wait_read();
+                bulk_wait_read<1>();  // warpgroup 0's half (in the Q tile) has been read
                 mbar_arrive(bar(C::kBarEmpty + s));
+                bulk_wait_read<0>();
+                mbar_arrive(bar(C::kBarEmptyDO + s));
             }
         }
       } else if (warp == kBwdMmaWarp) {
@@ -389,11 +414,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const uint32_t sQ = stage_q(it);
                 const uint32_t sDO = stage_do(it);
                 // dP^T = V dO^T (d = 128: into the columns the previous dQ occupied)
+                ok = bwd_wait(bar(C::kBarFullDO + it % C::kStages), (it / C::kStages) & 1, abort_flag, p, 34);
+                if (!ok) break;
                 if (!C::kDqOwnCols && it > 0) {
                     ok = bwd_wait(bar(C::kBarDQFree), (it - 1) & 1, abort_flag, p, 35);
                     if (!ok) break;
-                    tc_fence_after();
                 }
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < C::kDSteps; ++kk)
                     mma_ss<false>(tDP, kmaj(sV, kk), kmaj(sDO, kk), C::kIdescS, kk > 0 ? 1u : 0u);
