@@ -78,7 +78,10 @@ struct BwdCfg {
     static constexpr int kUmmaK = 16;
     static constexpr int kDSteps = D / kUmmaK;           // k-steps of S^T and dP^T (over d)
     static constexpr int kRowSteps = 128 / kUmmaK;       // k-steps over 128 query rows or keys
-    static constexpr int kStages = 2;
+    // Q/dO stages: the stage of tile j is handed back only when tile j's dQ
+    // reduction (staged in it) has been read, so deeper rings hide that
+    // latency; d = 128 fits two stages, d = 64 four.
+    static constexpr int kStages = D == 64 ? 4 : 2;
     static constexpr uint32_t kFmt = F16 ? 0u : 1u;
     // S^T = K Q^T and dP^T = V dO^T: M = 128 keys, N = 128 query rows, both K-major.
     static constexpr uint32_t kIdescS = instr_desc(kFmt, false, false, 128, 128);
