@@ -93,6 +93,10 @@ def load(path: str | None = None):
                                          c_int, vp]
         lib.fa_fwd_ex_static_capacity.restype = sz
         lib.fa_fwd_ex_static_capacity.argtypes = []
+        lib.fa_fwd_host.restype = c_int
+        lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, c_int, vp, sz, vp]
+        lib.fa_fwd_host_workspace_size.restype = sz
+        lib.fa_fwd_host_workspace_size.argtypes = [i64, i64, i64, i64, i64, i64, c_int]
         bwd_args = [vp] * 9 + [i64] * 6 + [f32, c_int, vp, sz]
         lib.fa_bwd.restype = c_int
         lib.fa_bwd.argtypes = bwd_args + [vp]
@@ -156,6 +160,17 @@ def fa_fwd_ex_static(q: int, k: int, v: int, o: int, lse: int | None, B: int, H:
 
 def fa_fwd_ex_static_capacity() -> int:
     return int(load().fa_fwd_ex_static_capacity())
+
+
+def fa_fwd_host(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, H_kv: int, N_q: int,
+                N_kv: int, d: int, scale: float, dtype: int, workspace: int | None, workspace_bytes: int,
+                stream: int | None) -> int:
+    return load().fa_fwd_host(q, k, v, o, lse, B, H, H_kv, N_q, N_kv, d, scale, dtype, workspace,
+                              workspace_bytes, stream)
+
+
+def fa_fwd_host_workspace_size(B: int, H: int, H_kv: int, N_q: int, N_kv: int, d: int, dtype: int) -> int:
+    return load().fa_fwd_host_workspace_size(B, H, H_kv, N_q, N_kv, d, dtype)
 
 
 def fa_bwd(q: int, k: int, v: int, o: int, dout: int, lse: int, dq: int, dk: int, dv: int, B: int,

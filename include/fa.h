@@ -178,6 +178,36 @@ int fa_fwd_ex_static(const void* q, const void* k, const void* v, void* o,
 size_t fa_fwd_ex_static_capacity(void);
 
 /*
+ * fa_fwd_host — fa_fwd_ex on tensors in HOST memory: the inputs are copied
+ * to the GPU, the forward pass runs, and o and lse are copied back, with the
+ * copies of one chunk of key/value heads overlapped with the computation of
+ * the previous one (three streams: the caller's `stream` for the kernels and
+ * two the library creates once per device).  Same arguments, layouts, dtypes,
+ * flags and checks as fa_fwd_ex with num_splits = 1, except:
+ *   q, k, v, o, lse : host memory; pinned (page-locked) memory is needed
+ *                     for the copies to overlap (pageable memory works but
+ *                     serialises them).
+ *   workspace       : caller-owned DEVICE memory of at least
+ *                     fa_fwd_host_workspace_size(...) bytes, 256-byte
+ *                     aligned (three chunk slots of q, k, v, o, lse).
+ * Completion: when `stream` reaches the point after this call, o and lse
+ * hold the results in host memory.  Calls on one device share the two
+ * internal streams (a mutex serialises their enqueueing).  Returns as
+ * fa_fwd_ex; FA_ERR_INVALID_ARG for a missing or short workspace,
+ * FA_ERR_ALIGNMENT for a workspace not 256-byte aligned.
+ * The pages have no counterpart of this entry point; it is the host-to-host
+ * form of the forward pass that end-to-end measurements call.
+ */
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv,
+                int64_t d, float scale, int dtype, void* workspace,
+                size_t workspace_bytes, void* stream);
+
+/* Device workspace bytes fa_fwd_host needs (0 for invalid sizes). */
+size_t fa_fwd_host_workspace_size(int64_t B, int64_t H, int64_t H_kv, int64_t N_q,
+                                  int64_t N_kv, int64_t d, int dtype);
+
+/*
  * fa_bwd — gradients of exact attention for an upstream gradient dO:
  *
  *   P = softmax(scale Q K^T) (recomputed from q, k and the saved lse),

@@ -180,3 +180,17 @@ def test_bwd_validation(lib):
     # rejected before any CUDA call
     assert fab.fa_bwd(Q, K, V, O, 6 << 32, L, 7 << 32, 8 << 32, 9 << 32, 2, 8, 2, 300, 333, 96, 0.125,
                       fab.FA_DTYPE_BF16, 10 << 32, 1 << 30, None) == fab.FA_ERR_UNSUPPORTED
+
+
+def test_host_pipeline_validation(lib):
+    code = fab.FA_DTYPE_BF16
+    need = fab.fa_fwd_host_workspace_size(2, 8, 2, 300, 300, 128, code)
+    assert need > 0 and fab.fa_fwd_host_workspace_size(2, 8, 3, 300, 300, 128, code) == 0
+    WS = 6 << 32
+    args = (Q, K, V, O, L, 2, 8, 2, 300, 300, 128, 0.088, code)
+    # rejected before any CUDA call
+    assert fab.fa_fwd_host(*args, None, need, None) == fab.FA_ERR_INVALID_ARG
+    assert fab.fa_fwd_host(*args, WS, need - 1, None) == fab.FA_ERR_INVALID_ARG
+    assert fab.fa_fwd_host(*args, WS + 16, need, None) == fab.FA_ERR_ALIGNMENT
+    assert fab.fa_fwd_host(Q, K, V, O, L, 2, 8, 2, 300, 300, 96, 0.088, code, WS, need, None) == \
+        fab.FA_ERR_UNSUPPORTED

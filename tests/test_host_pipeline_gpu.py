@@ -1,0 +1,68 @@
+"""fa_fwd_host: the forward pass on host tensors with overlapped copies.
+
+Each chunk is an ordinary fa_fwd_ex launch on device copies of contiguous
+head ranges, so the outputs must equal fa_fwd_ex on the whole problem bit for
+bit; they are also compared with the oracle on sampled rows."""
+import numpy as np
+import pytest
+
+from exact_tiled_attention_04_gb300 import binding as fab
+from exact_tiled_attention_04_gb300 import inputs as I
+
+from .gpu_util import DTYPE_CODES, TOL_LSE, compare_ex, ensure_library, run_fa_ex, to_device, tol_o_dtype
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return ensure_library()
+
+
+def run_host(q, k, v, dtype, causal=False, with_lse=True):
+    B, H, Nq, d = q.shape
+    H_kv, Nkv = k.shape[1], k.shape[2]
+    hq, hk, hv = (to_device(x, dtype).cpu().pin_memory() for x in (q, k, v))
+    ho = torch.full_like(hq, float("nan")).pin_memory()
+    hl = torch.full((B, H, Nq), float("nan"), dtype=torch.float32).pin_memory() if with_lse else None
+    code = DTYPE_CODES[dtype] | (fab.FA_FLAG_CAUSAL if causal else 0)
+    need = fab.fa_fwd_host_workspace_size(B, H, H_kv, Nq, Nkv, d, code)
+    ws = torch.empty(need + 256, dtype=torch.uint8, device="cuda")
+    base = (ws.data_ptr() + 255) // 256 * 256
+    sc = float(np.float32(1.0 / np.sqrt(d)))
+    s = torch.cuda.current_stream()
+    st = fab.fa_fwd_host(hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), ho.data_ptr(),
+                         hl.data_ptr() if hl is not None else None, B, H, H_kv, Nq, Nkv, d, sc, code, base,
+                         need, s.cuda_stream)
+    assert st == fab.FA_OK, (st, fab.fa_last_error_message())
+    assert fab.fa_device_status(s.cuda_stream) == fab.FA_OK
+    return ho.float().numpy(), (hl.numpy() if hl is not None else None)
+
+
+@pytest.mark.parametrize("B,H,H_kv,Nq,Nkv,d,dtype,causal", [
+    (1, 1, 1, 300, 333, 64, "bf16", False),      # one chunk
+    (1, 3, 3, 200, 200, 128, "bf16", True),      # fewer chunks than slots
+    (3, 12, 6, 130, 260, 64, "f16", False),      # 18 units: 9 chunks of 2
+    (2, 17, 17, 257, 129, 128, "bf16", True),    # ragged last chunk
+    (4, 16, 4, 1, 700, 128, "bf16", False),      # decode: packed grouped heads
+    (2, 4, 4, 160, 160, 64, "f32", False),       # TF32 path
+])
+def test_matches_device_call(B, H, H_kv, Nq, Nkv, d, dtype, causal):
+    q, k, v = I.make_general(B, H, H_kv, Nq, Nkv, d, dtype, seed=700 + H + Nq)
+    o_h, l_h = run_host(q, k, v, dtype, causal)
+    o_d, l_d = run_fa_ex(q, k, v, dtype, 1, causal=causal)
+    assert np.array_equal(o_h, o_d) and np.array_equal(l_h, l_d)
+    rng = np.random.default_rng(5)
+    rows = np.stack([rng.integers(0, B, 16), rng.integers(0, H, 16), rng.integers(0, Nq, 16)], axis=1)
+    err_o, err_l = compare_ex(dtype, o_h, l_h, q, k, v, rows=rows, causal=causal)
+    assert err_o <= tol_o_dtype(dtype) and err_l <= TOL_LSE
+
+
+def test_without_lse_and_repeated():
+    q, k, v = I.make_general(2, 8, 2, 300, 300, 128, "bf16", seed=710)
+    o1, _ = run_host(q, k, v, "bf16", with_lse=False)
+    o2, l2 = run_host(q, k, v, "bf16")
+    assert np.array_equal(o1, o2) and np.isfinite(l2).all()
