@@ -288,8 +288,9 @@ def run_reference(args, w):
 
 def config_of(w, n_gpus: int, splits: int = 1):
     nbytes = w.bytes()
-    l2 = (f"inputs larger than L2: q,k,v,o,lse = {nbytes / 1e6:.0f} MB per step (L2 129 MB), no flush"
-          if nbytes > 129e6 else f"L2-resident: q,k,v,o,lse = {nbytes / 1e6:.1f} MB per step")
+    what = "q,k,v,o,dO,lse,dq,dk,dv" if w.backward else "q,k,v,o,lse"
+    l2 = (f"inputs larger than L2: {what} = {nbytes / 1e6:.0f} MB per step (L2 129 MB), no flush"
+          if nbytes > 129e6 else f"L2-resident: {what} = {nbytes / 1e6:.1f} MB per step")
     cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype,
            "inputs": f"seeded N(0,1) x {w.factor}", "scale": float(w.scale), "l2": l2,
            "parallelism": f"independent replica per GPU x{n_gpus}"}
