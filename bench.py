@@ -16,7 +16,7 @@ steps, inputs resident in HBM; 539 MB of inputs+outputs per step exceed the
 129 MB L2).  `e2e` is the same metric through fa_fwd_host, the C-ABI call on
 HOST tensors (pinned): each step copies Q, K, V to the GPU and O, lse back,
 overlapped with the computation chunk by chunk inside the call (backward
-workloads: explicit copies of their inputs and gradients around fa_bwd).  `roofline` compares the kernel with the measured dense bf16
+workloads: fa_bwd_host the same way).  `roofline` compares the kernel with the measured dense bf16
 tensor peak.  `cpu_baseline` times the fp64 CPU oracle on a bounded sample of
 the same workload on the host cores (rank 0 only).
 
@@ -392,20 +392,23 @@ def run_ours(args, w):
             if st != fab.FA_OK:
                 raise fab.FAError(st, "fa_bwd")
 
-        # end to end: q, k, v, o, dO, lse up; dq, dk, dv back
-        h2d_pairs = [(dq, hq), (dk, hk), (dv, hv), (do, ho), (ddout, hdout), (dlse, hl)]
+        # end to end: fa_bwd_host on pinned host tensors (q, k, v, o, dO, lse
+        # up; dq, dk, dv back, overlapped with the computation inside the call)
         hgq, hgk, hgv = (torch.empty_like(t).pin_memory() for t in (hq, hk, hv))
-        d2h_pairs = [(hgq, gq), (hgk, gk), (hgv, gv)]
+        host_bytes = fab.fa_bwd_host_workspace_size(w.B, w.H, w.H_kv, w.N, w.Nkv, w.d)
+        host_work = torch.empty(host_bytes + 256, dtype=torch.uint8, device=dev)
+        host_ws = (host_work.data_ptr() + 255) // 256 * 256
+        host_in = (hq, hk, hv, ho, hdout, hl)
 
         def e2e_step():
-            for dst, src in h2d_pairs:
-                dst.copy_(src, non_blocking=True)
-            step_fn()
-            for dst, src in d2h_pairs:
-                dst.copy_(src, non_blocking=True)
+            st = fab.fa_bwd_host(*(t.data_ptr() for t in host_in), hgq.data_ptr(), hgk.data_ptr(),
+                                 hgv.data_ptr(), w.B, w.H, w.H_kv, w.N, w.Nkv, w.d, scale, dt_code, host_ws,
+                                 host_bytes, sp)
+            if st != fab.FA_OK:
+                raise fab.FAError(st, "fa_bwd_host")
 
-        h2d = sum(h.numel() * h.element_size() for _, h in h2d_pairs)
-        d2h = sum(h.numel() * h.element_size() for h, _ in d2h_pairs)
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in (hgq, hgk, hgv))
 
     def step():
         nonlocal launches

@@ -104,6 +104,10 @@ def load(path: str | None = None):
         lib.fa_bwd_validate.argtypes = bwd_args
         lib.fa_bwd_workspace_size.restype = sz
         lib.fa_bwd_workspace_size.argtypes = [i64, i64, i64, i64]
+        lib.fa_bwd_host.restype = c_int
+        lib.fa_bwd_host.argtypes = bwd_args + [vp]
+        lib.fa_bwd_host_workspace_size.restype = sz
+        lib.fa_bwd_host_workspace_size.argtypes = [i64, i64, i64, i64, i64, i64]
         _lib = lib
         return lib
 
@@ -189,6 +193,17 @@ def fa_bwd_validate(q: int, k: int, v: int, o: int, dout: int, lse: int, dq: int
 
 def fa_bwd_workspace_size(B: int, H: int, N_q: int, d: int) -> int:
     return load().fa_bwd_workspace_size(B, H, N_q, d)
+
+
+def fa_bwd_host(q: int, k: int, v: int, o: int, dout: int, lse: int, dq: int, dk: int, dv: int, B: int,
+                H: int, H_kv: int, N_q: int, N_kv: int, d: int, scale: float, dtype: int,
+                workspace: int | None, workspace_bytes: int, stream: int | None) -> int:
+    return load().fa_bwd_host(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, N_q, N_kv, d, scale, dtype,
+                              workspace, workspace_bytes, stream)
+
+
+def fa_bwd_host_workspace_size(B: int, H: int, H_kv: int, N_q: int, N_kv: int, d: int) -> int:
+    return load().fa_bwd_host_workspace_size(B, H, H_kv, N_q, N_kv, d)
 
 
 def fa_device_status(stream: int | None) -> int:

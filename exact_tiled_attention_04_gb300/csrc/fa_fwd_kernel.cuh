@@ -443,7 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool pack = kOneTile || p.pack != 0;
     const unsigned int split = blockIdx.x % static_cast<unsigned>(p.splits);
     const unsigned int cta = blockIdx.x / static_cast<unsigned>(p.splits);
-    const int qb = static_cast<int>(cta % static_cast<unsigned>(p.n_q_blocks));
+    // causal: later query blocks see more keys; they are launched first
+    const int qb_lin = static_cast<int>(cta % static_cast<unsigned>(p.n_q_blocks));
+    const int qb = kCausal ? p.n_q_blocks - 1 - qb_lin : qb_lin;
     const int bh = static_cast<int>(cta / static_cast<unsigned>(p.n_q_blocks));
     // key/value head of this query head (grouped-query attention: H / H_kv
     // query heads share one key/value head)

@@ -1,13 +1,13 @@
-// fa_fwd_host: the forward pass on tensors in host memory, with the copies
-// to and from the GPU overlapped with the computation (declared in
-// include/fa.h).
+// fa_fwd_host / fa_bwd_host: the forward and backward passes on tensors in
+// host memory, with the copies to and from the GPU overlapped with the
+// computation (declared in include/fa.h).
 //
 // The work is cut into chunks of consecutive key/value heads (with their
 // query heads), at most eight and each large enough to keep about 256 CTAs
 // (one chunk for small problems).  In the flattened [B*H_kv] head order, a
 // chunk's q, o and lse rows and its k, v rows are each one contiguous range,
 // so each chunk is an ordinary fa_fwd_ex call on device copies of those
-// ranges.  Three streams:
+// ranges (fa_bwd for the backward pass).  Three streams:
 // copies in, the caller's stream for the kernels, copies out; chunk slots in
 // the caller's workspace form a ring so chunk c+1 arrives while chunk c is
 // computed and chunk c-1 leaves.  The caller's stream is made to wait for the
@@ -15,6 +15,7 @@
 // memory.
 #include <cstddef>
 #include <cstdint>
+#include <functional>
 #include <mutex>
 
 #include "fa.h"
@@ -66,8 +67,74 @@ int device_streams(DeviceStreams** out, int* dev_out) {
 
 size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 
-// The chunking of a problem: units (key/value heads, flattened over the
-// batch) per chunk, and the bytes of one slot.
+// One chunk's work: copies in (host -> device), the kernels (enqueued on the
+// caller's stream by `compute`), copies out (device -> host).
+struct Copy {
+    void* dst;
+    const void* src;
+    size_t bytes;
+};
+struct ChunkWork {
+    Copy in[8];
+    int n_in = 0;
+    Copy out[4];
+    int n_out = 0;
+    std::function<int()> compute;
+};
+
+// Runs `chunks` chunks through `slots` workspace slots: chunk c's copies in
+// wait for slot c % slots to be freed by chunk c - slots's copies out.  The
+// caller's stream waits for the last copies out at the end.
+int run_pipeline(DeviceStreams* ds, cudaStream_t s, int64_t chunks, int slots,
+                 const std::function<void(int64_t, int, ChunkWork&)>& make) {
+    auto fail = [&](const char* what, cudaError_t e) {
+        set_error(what, static_cast<int>(e), cudaGetErrorString(e));
+        return FA_ERR_CUDA;
+    };
+    // the first copies in may only write the workspace once earlier work on
+    // the caller's stream (which may still read it) is done
+    cudaError_t e = cudaEventRecord(ds->computed[0], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->in, ds->computed[0], 0);
+    if (e != cudaSuccess) return fail("pipeline start", e);
+    for (int64_t c = 0; c < chunks; ++c) {
+        const int slot = static_cast<int>(c % slots);
+        ChunkWork w;
+        make(c, slot, w);
+        if (c >= slots && (e = cudaStreamWaitEvent(ds->in, ds->freed[slot], 0)) != cudaSuccess)
+            return fail("pipeline wait (slot)", e);
+        for (int i = 0; i < w.n_in; ++i)
+            if ((e = cudaMemcpyAsync(w.in[i].dst, w.in[i].src, w.in[i].bytes, cudaMemcpyHostToDevice, ds->in)) !=
+                cudaSuccess)
+                return fail("pipeline copy in", e);
+        if ((e = cudaEventRecord(ds->loaded[slot], ds->in)) != cudaSuccess) return fail("pipeline record", e);
+        if ((e = cudaStreamWaitEvent(s, ds->loaded[slot], 0)) != cudaSuccess) return fail("pipeline wait (in)", e);
+        const int st = w.compute();
+        if (st != FA_OK) return st;
+        if ((e = cudaEventRecord(ds->computed[slot], s)) != cudaSuccess) return fail("pipeline record", e);
+        if ((e = cudaStreamWaitEvent(ds->out, ds->computed[slot], 0)) != cudaSuccess)
+            return fail("pipeline wait (computed)", e);
+        for (int i = 0; i < w.n_out; ++i)
+            if ((e = cudaMemcpyAsync(w.out[i].dst, w.out[i].src, w.out[i].bytes, cudaMemcpyDeviceToHost,
+                                     ds->out)) != cudaSuccess)
+                return fail("pipeline copy out", e);
+        if ((e = cudaEventRecord(ds->freed[slot], ds->out)) != cudaSuccess) return fail("pipeline record", e);
+    }
+    const int last = static_cast<int>((chunks - 1) % slots);
+    if ((e = cudaStreamWaitEvent(s, ds->freed[last], 0)) != cudaSuccess) return fail("pipeline end", e);
+    return FA_OK;
+}
+
+// Chunks of consecutive key/value heads (units) keeping about kChunkCtas
+// CTAs each, at most kMaxChunks.
+int64_t chunk_count(int64_t units, int64_t ctas_per_unit) {
+    int64_t chunks = units * ctas_per_unit / kChunkCtas;
+    if (chunks > kMaxChunks) chunks = kMaxChunks;
+    if (chunks > units) chunks = units;
+    return chunks < 1 ? 1 : chunks;
+}
+
+// The forward chunking: units per chunk and the bytes of one slot
+// (q, o, k, v, lse and split partials of a chunk).
 struct Plan {
     int64_t units = 0, per_chunk = 0, chunks = 0;
     size_t q_bytes = 0, kv_bytes = 0, lse_bytes = 0, split_bytes = 0;  // per chunk
@@ -79,14 +146,9 @@ Plan make_plan(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, in
     const int64_t group = H / H_kv;
     const size_t elem = (dtype & 0xFF) == FA_DTYPE_F32 ? 4 : 2;
     pl.units = B * H_kv;
-    // as many chunks as keep each launch about kChunkCtas CTAs (a chunk that
-    // underfills the GPU computes slower than the copies it would hide)
+    // a chunk that underfills the GPU computes slower than the copies it would hide
     const bool packed = group > 1 && N_q * group <= 128;
-    const int64_t ctas_per_unit = packed ? 1 : group * ((N_q + 255) / 256);
-    int64_t chunks = pl.units * ctas_per_unit / kChunkCtas;
-    if (chunks > kMaxChunks) chunks = kMaxChunks;
-    if (chunks > pl.units) chunks = pl.units;
-    if (chunks < 1) chunks = 1;
+    const int64_t chunks = chunk_count(pl.units, packed ? 1 : group * ((N_q + 255) / 256));
     pl.per_chunk = (pl.units + chunks - 1) / chunks;
     pl.chunks = (pl.units + pl.per_chunk - 1) / pl.per_chunk;
     const size_t qh = static_cast<size_t>(pl.per_chunk * group);
@@ -96,6 +158,31 @@ Plan make_plan(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, in
     pl.split_bytes = fa_fwd_ex_workspace_size(1, static_cast<int64_t>(qh), N_q, N_kv, d, 1);
     pl.slot_bytes = 2 * align256(pl.q_bytes) + 2 * align256(pl.kv_bytes) + align256(pl.lse_bytes) +
                     align256(pl.split_bytes);
+    return pl;
+}
+
+// The backward chunking: slot = q, o, dO, dq, k, v, dk, dv, lse and the
+// chunk's fa_bwd workspace.
+struct BwdPlan {
+    int64_t units = 0, per_chunk = 0, chunks = 0;
+    size_t q_bytes = 0, kv_bytes = 0, lse_bytes = 0, ws_bytes = 0;
+    size_t slot_bytes = 0;
+};
+
+BwdPlan make_bwd_plan(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d) {
+    BwdPlan pl;
+    const int64_t group = H / H_kv;
+    pl.units = B * H_kv;
+    const int64_t chunks = chunk_count(pl.units, (N_kv + 127) / 128);  // one CTA per 128 keys of a unit
+    pl.per_chunk = (pl.units + chunks - 1) / chunks;
+    pl.chunks = (pl.units + pl.per_chunk - 1) / pl.per_chunk;
+    const size_t qh = static_cast<size_t>(pl.per_chunk * group);
+    pl.q_bytes = qh * static_cast<size_t>(N_q) * static_cast<size_t>(d) * 2;
+    pl.kv_bytes = static_cast<size_t>(pl.per_chunk) * static_cast<size_t>(N_kv) * static_cast<size_t>(d) * 2;
+    pl.lse_bytes = qh * static_cast<size_t>(N_q) * sizeof(float);
+    pl.ws_bytes = fa_bwd_workspace_size(1, static_cast<int64_t>(qh), N_q, d);
+    pl.slot_bytes = 4 * align256(pl.q_bytes) + 4 * align256(pl.kv_bytes) + align256(pl.lse_bytes) +
+                    align256(pl.ws_bytes);
     return pl;
 }
 
@@ -135,66 +222,94 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
     const size_t q_head = static_cast<size_t>(N_q) * static_cast<size_t>(d) * elem;
     const size_t kv_head = static_cast<size_t>(N_kv) * static_cast<size_t>(d) * elem;
     const size_t lse_head = static_cast<size_t>(N_q) * sizeof(float);
-    auto fail = [&](const char* what, cudaError_t e) {
-        set_error(what, static_cast<int>(e), cudaGetErrorString(e));
-        return FA_ERR_CUDA;
-    };
-
-    // the inputs of the first chunk may only be written once earlier work on
-    // the caller's stream that may read the workspace is done
-    cudaError_t e = cudaEventRecord(ds->computed[0], s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(ds->in, ds->computed[0], 0);
-    if (e != cudaSuccess) return fail("pipeline start", e);
-
-    for (int64_t c = 0; c < pl.chunks; ++c) {
-        const int slot = static_cast<int>(c % slots);
+    return run_pipeline(ds, s, pl.chunks, slots, [&](int64_t c, int slot, ChunkWork& w) {
         const int64_t u0 = c * pl.per_chunk;
         const int64_t nu = (u0 + pl.per_chunk <= pl.units) ? pl.per_chunk : pl.units - u0;
         const int64_t hq0 = u0 * group, nq = nu * group;  // query heads of the chunk (flattened)
-        uint8_t* base = static_cast<uint8_t*>(workspace) + static_cast<size_t>(slot) * pl.slot_bytes;
-        uint8_t* dq = base;
+        uint8_t* dq = static_cast<uint8_t*>(workspace) + static_cast<size_t>(slot) * pl.slot_bytes;
         uint8_t* dout = dq + align256(pl.q_bytes);
         uint8_t* dk = dout + align256(pl.q_bytes);
         uint8_t* dv = dk + align256(pl.kv_bytes);
         float* dl = reinterpret_cast<float*>(dv + align256(pl.kv_bytes));
         uint8_t* dsplit = reinterpret_cast<uint8_t*>(dl) + align256(pl.lse_bytes);
-
-        // copies in, once the slot's previous chunk has left
-        if (c >= slots && (e = cudaStreamWaitEvent(ds->in, ds->freed[slot], 0)) != cudaSuccess)
-            return fail("pipeline wait (slot)", e);
         const size_t qb = static_cast<size_t>(nq) * q_head, kvb = static_cast<size_t>(nu) * kv_head;
-        if ((e = cudaMemcpyAsync(dq, static_cast<const uint8_t*>(q) + static_cast<size_t>(hq0) * q_head, qb,
-                                 cudaMemcpyHostToDevice, ds->in)) != cudaSuccess ||
-            (e = cudaMemcpyAsync(dk, static_cast<const uint8_t*>(k) + static_cast<size_t>(u0) * kv_head, kvb,
-                                 cudaMemcpyHostToDevice, ds->in)) != cudaSuccess ||
-            (e = cudaMemcpyAsync(dv, static_cast<const uint8_t*>(v) + static_cast<size_t>(u0) * kv_head, kvb,
-                                 cudaMemcpyHostToDevice, ds->in)) != cudaSuccess ||
-            (e = cudaEventRecord(ds->loaded[slot], ds->in)) != cudaSuccess)
-            return fail("pipeline copy in", e);
+        w.in[w.n_in++] = {dq, static_cast<const uint8_t*>(q) + static_cast<size_t>(hq0) * q_head, qb};
+        w.in[w.n_in++] = {dk, static_cast<const uint8_t*>(k) + static_cast<size_t>(u0) * kv_head, kvb};
+        w.in[w.n_in++] = {dv, static_cast<const uint8_t*>(v) + static_cast<size_t>(u0) * kv_head, kvb};
+        w.compute = [=]() {
+            return fa_fwd_ex(dq, dk, dv, dout, lse != nullptr ? dl : nullptr, 1, nq, nu, N_q, N_kv, d, scale, dtype,
+                             1, pl.split_bytes ? dsplit : nullptr, pl.split_bytes, s);
+        };
+        w.out[w.n_out++] = {static_cast<uint8_t*>(o) + static_cast<size_t>(hq0) * q_head, dout, qb};
+        if (lse != nullptr)
+            w.out[w.n_out++] = {reinterpret_cast<uint8_t*>(lse) + static_cast<size_t>(hq0) * lse_head, dl,
+                                static_cast<size_t>(nq) * lse_head};
+    });
+}
 
-        // the chunk's forward pass on the caller's stream
-        if ((e = cudaStreamWaitEvent(s, ds->loaded[slot], 0)) != cudaSuccess) return fail("pipeline wait (in)", e);
-        st = fa_fwd_ex(dq, dk, dv, dout, lse != nullptr ? dl : nullptr, 1, nq, nu, N_q, N_kv, d, scale, dtype, 1,
-                       pl.split_bytes ? dsplit : nullptr, pl.split_bytes, s);
-        if (st != FA_OK) return st;
-        if ((e = cudaEventRecord(ds->computed[slot], s)) != cudaSuccess) return fail("pipeline record", e);
+size_t fa_bwd_host_workspace_size(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d) {
+    if (B < 1 || H < 1 || H_kv < 1 || H % H_kv != 0 || N_q < 1 || N_kv < 1 || (d != 64 && d != 128)) return 0;
+    if (B > INT64_MAX / H || B * H > INT64_MAX / (N_q + 128) || B * H * (N_q + 128) > INT64_MAX / (d * 4)) return 0;
+    if (B * H_kv > INT64_MAX / N_kv || B * H_kv * N_kv > INT64_MAX / (d * 4)) return 0;
+    const BwdPlan pl = make_bwd_plan(B, H, H_kv, N_q, N_kv, d);
+    return static_cast<size_t>(pl.chunks < kSlots ? pl.chunks : kSlots) * pl.slot_bytes;
+}
 
-        // copies out
-        if ((e = cudaStreamWaitEvent(ds->out, ds->computed[slot], 0)) != cudaSuccess ||
-            (e = cudaMemcpyAsync(static_cast<uint8_t*>(o) + static_cast<size_t>(hq0) * q_head, dout, qb,
-                                 cudaMemcpyDeviceToHost, ds->out)) != cudaSuccess)
-            return fail("pipeline copy out", e);
-        if (lse != nullptr &&
-            (e = cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse) + static_cast<size_t>(hq0) * lse_head, dl,
-                                 static_cast<size_t>(nq) * lse_head, cudaMemcpyDeviceToHost, ds->out)) !=
-                cudaSuccess)
-            return fail("pipeline copy out (lse)", e);
-        if ((e = cudaEventRecord(ds->freed[slot], ds->out)) != cudaSuccess) return fail("pipeline record", e);
-    }
-    // completion on the caller's stream: every copy out has finished
-    const int last = static_cast<int>((pl.chunks - 1) % slots);
-    if ((e = cudaStreamWaitEvent(s, ds->freed[last], 0)) != cudaSuccess) return fail("pipeline end", e);
-    return FA_OK;
+int fa_bwd_host(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv,
+                int64_t d, float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    if (workspace == nullptr) return FA_ERR_INVALID_ARG;
+    // the argument checks of fa_bwd on the whole problem (host pointers);
+    // the device workspace is checked against this call's own size below
+    int st = fa_bwd_validate(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, N_q, N_kv, d, scale, dtype, workspace,
+                             fa_bwd_workspace_size(B, H, N_q, d));
+    if (st != FA_OK) return st;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGNMENT;
+    const BwdPlan pl = make_bwd_plan(B, H, H_kv, N_q, N_kv, d);
+    const int slots = static_cast<int>(pl.chunks < kSlots ? pl.chunks : kSlots);
+    if (workspace_bytes < static_cast<size_t>(slots) * pl.slot_bytes) return FA_ERR_INVALID_ARG;
+
+    DeviceStreams* ds = nullptr;
+    int dev = 0;
+    if ((st = device_streams(&ds, &dev)) != FA_OK) return st;
+    std::lock_guard<std::mutex> lock(g_streams_mutex[dev]);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t group = H / H_kv;
+    const size_t q_head = static_cast<size_t>(N_q) * static_cast<size_t>(d) * 2;
+    const size_t kv_head = static_cast<size_t>(N_kv) * static_cast<size_t>(d) * 2;
+    const size_t lse_head = static_cast<size_t>(N_q) * sizeof(float);
+    return run_pipeline(ds, s, pl.chunks, slots, [&](int64_t c, int slot, ChunkWork& w) {
+        const int64_t u0 = c * pl.per_chunk;
+        const int64_t nu = (u0 + pl.per_chunk <= pl.units) ? pl.per_chunk : pl.units - u0;
+        const int64_t hq0 = u0 * group, nq = nu * group;
+        uint8_t* p0 = static_cast<uint8_t*>(workspace) + static_cast<size_t>(slot) * pl.slot_bytes;
+        uint8_t* d_q = p0;
+        uint8_t* d_o = d_q + align256(pl.q_bytes);
+        uint8_t* d_do = d_o + align256(pl.q_bytes);
+        uint8_t* d_dq = d_do + align256(pl.q_bytes);
+        uint8_t* d_k = d_dq + align256(pl.q_bytes);
+        uint8_t* d_v = d_k + align256(pl.kv_bytes);
+        uint8_t* d_dk = d_v + align256(pl.kv_bytes);
+        uint8_t* d_dv = d_dk + align256(pl.kv_bytes);
+        float* d_l = reinterpret_cast<float*>(d_dv + align256(pl.kv_bytes));
+        uint8_t* d_ws = reinterpret_cast<uint8_t*>(d_l) + align256(pl.lse_bytes);
+        const size_t qb = static_cast<size_t>(nq) * q_head, kvb = static_cast<size_t>(nu) * kv_head;
+        const size_t qoff = static_cast<size_t>(hq0) * q_head, kvoff = static_cast<size_t>(u0) * kv_head;
+        w.in[w.n_in++] = {d_q, static_cast<const uint8_t*>(q) + qoff, qb};
+        w.in[w.n_in++] = {d_o, static_cast<const uint8_t*>(o) + qoff, qb};
+        w.in[w.n_in++] = {d_do, static_cast<const uint8_t*>(dout) + qoff, qb};
+        w.in[w.n_in++] = {d_k, static_cast<const uint8_t*>(k) + kvoff, kvb};
+        w.in[w.n_in++] = {d_v, static_cast<const uint8_t*>(v) + kvoff, kvb};
+        w.in[w.n_in++] = {d_l, reinterpret_cast<const uint8_t*>(lse) + static_cast<size_t>(hq0) * lse_head,
+                          static_cast<size_t>(nq) * lse_head};
+        w.compute = [=]() {
+            return fa_bwd(d_q, d_k, d_v, d_o, d_do, d_l, d_dq, d_dk, d_dv, 1, nq, nu, N_q, N_kv, d, scale, dtype,
+                          d_ws, pl.ws_bytes, s);
+        };
+        w.out[w.n_out++] = {static_cast<uint8_t*>(dq) + qoff, d_dq, qb};
+        w.out[w.n_out++] = {static_cast<uint8_t*>(dk) + kvoff, d_dk, kvb};
+        w.out[w.n_out++] = {static_cast<uint8_t*>(dv) + kvoff, d_dv, kvb};
+    });
 }
 
 }  // extern "C"

@@ -252,6 +252,27 @@ int fa_bwd_validate(const void* q, const void* k, const void* v, const void* o,
                     int64_t N_kv, int64_t d, float scale, int dtype,
                     const void* workspace, size_t workspace_bytes);
 
+/*
+ * fa_bwd_host — fa_bwd on tensors in HOST memory (q, k, v, o, dout, lse in;
+ * dq, dk, dv out), with the copies of one chunk of key/value heads
+ * overlapped with the computation of the previous one, as fa_fwd_host does
+ * (it shares that entry point's two internal streams).  Same arguments,
+ * layouts, dtypes, flags and checks as fa_bwd, except: the tensors are host
+ * memory (pinned for the copies to overlap), and `workspace` is device
+ * memory of at least fa_bwd_host_workspace_size(...) bytes, 256-byte
+ * aligned.  Completion on `stream` means dq, dk, dv are in host memory.
+ * The pages have no counterpart of this entry point.
+ */
+int fa_bwd_host(const void* q, const void* k, const void* v, const void* o,
+                const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv,
+                int64_t d, float scale, int dtype, void* workspace,
+                size_t workspace_bytes, void* stream);
+
+/* Device workspace bytes fa_bwd_host needs (0 for invalid sizes). */
+size_t fa_bwd_host_workspace_size(int64_t B, int64_t H, int64_t H_kv, int64_t N_q,
+                                  int64_t N_kv, int64_t d);
+
 /* Workspace bytes fa_bwd needs (0 for invalid sizes):
    8 * B * H * ceil(N_q / 128) * 128 (rounded up to 256) + 4 * B * H * N_q * d. */
 size_t fa_bwd_workspace_size(int64_t B, int64_t H, int64_t N_q, int64_t d);

@@ -66,3 +66,41 @@ def test_without_lse_and_repeated():
     o1, _ = run_host(q, k, v, "bf16", with_lse=False)
     o2, l2 = run_host(q, k, v, "bf16")
     assert np.array_equal(o1, o2) and np.isfinite(l2).all()
+
+
+@pytest.mark.parametrize("B,H,H_kv,Nq,Nkv,d,dtype,causal", [
+    (1, 2, 2, 300, 333, 64, "bf16", False),      # one chunk
+    (2, 8, 2, 200, 260, 128, "bf16", True),      # grouped heads
+    (4, 16, 16, 256, 1024, 64, "f16", False),    # several chunks
+])
+def test_backward_matches_device_call(B, H, H_kv, Nq, Nkv, d, dtype, causal):
+    """fa_bwd_host equals fa_bwd on device copies up to the summation order
+    of the dQ reductions (and the oracle within the gradient tolerance)."""
+    import oracle
+    from .gpu_util import grad_errors, run_bwd, tol_grad
+    q, k, v = I.make_general(B, H, H_kv, Nq, Nkv, d, dtype, seed=720 + H + Nq)
+    dout = I.make_dout(B, H, Nq, d, dtype, seed=720 + H + Nq)
+    sc = float(np.float32(1.0 / np.sqrt(d)))
+    code = DTYPE_CODES[dtype] | (fab.FA_FLAG_CAUSAL if causal else 0)
+    # forward on the device for o and lse, then both backward forms
+    (gq, gk, gv), _ = run_bwd(q, k, v, dout, dtype, causal=causal)
+    tq, tk, tv, tdo = (to_device(x, dtype) for x in (q, k, v, dout))
+    o = torch.empty_like(tq)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
+    s = torch.cuda.current_stream()
+    assert fab.fa_fwd_ex(tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, H_kv,
+                         Nq, Nkv, d, sc, code, 1, None, 0, s.cuda_stream) == fab.FA_OK
+    hin = [t.cpu().pin_memory() for t in (tq, tk, tv, o, tdo, lse)]
+    hout = [torch.full_like(t, float("nan")).pin_memory() for t in (hin[0], hin[1], hin[2])]
+    need = fab.fa_bwd_host_workspace_size(B, H, H_kv, Nq, Nkv, d)
+    ws = torch.empty(need + 256, dtype=torch.uint8, device="cuda")
+    base = (ws.data_ptr() + 255) // 256 * 256
+    st = fab.fa_bwd_host(*(t.data_ptr() for t in hin), *(t.data_ptr() for t in hout), B, H, H_kv, Nq, Nkv, d,
+                         sc, code, base, need, s.cuda_stream)
+    assert st == fab.FA_OK, (st, fab.fa_last_error_message())
+    assert fab.fa_device_status(s.cuda_stream) == fab.FA_OK
+    got = [t.float().numpy() for t in hout]
+    for a, r in zip(got, (gq, gk, gv)):
+        assert np.max(np.abs(a - r)) <= 1e-2 * max(np.max(np.abs(r)), 1e-30)  # a bf16/fp16 ulp or so
+    errs = grad_errors(got, oracle.attention_bwd_f64(q, k, v, dout, sc, causal=causal))
+    assert max(errs) <= tol_grad(dtype), errs
