@@ -6,8 +6,10 @@
 One step = one fa_fwd call over the whole workload (every (batch, head) and
 every query row): the complete hot path.  Backward workloads (bwd_*): one
 step = one fa_bwd call (dQ, dK, dV for a seeded dO, three kernels) on the
-forward outputs computed once before timing; 10*B*H*N^2*d flops per step.  Default workload: B=2, H=32,
-N=8192, d=128, bf16 inputs drawn N(0,1)*0.5 from a seed (the compute-bound
+forward outputs computed once before timing; 10*B*H*N^2*d flops per step.
+The K timed steps are captured once into a CUDA graph and replayed (the
+same kernels, without the host's per-call work between them; --no-graph
+times plain launches).  Default workload: B=2, H=32, N=8192, d=128, bf16 inputs drawn N(0,1)*0.5 from a seed (the compute-bound
 headline shape).  The metric is attention-forward TFLOP/s counting
 4*B*H*N^2*d flops per step.
 
@@ -155,7 +157,20 @@ class ClockSampler:
                 stdout=self.file, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+        # start timing only once the sampler produces rows
+        t0 = time.time()
+        while self.proc is not None and self.count() == 0 and time.time() - t0 < 3.0:
+            time.sleep(0.01)
+        self.start_rows = self.count()
         return self
+
+    def count(self) -> int:
+        """Rows written so far."""
+        try:
+            with open(self.file.name) as f:
+                return sum(1 for r in f if r.strip())
+        except OSError:
+            return 0
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -190,6 +205,9 @@ class ClockSampler:
             for name, val in zip(names[1:], parts[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
+        # rows written before the timed region started are left out
+        skip = min(getattr(self, "start_rows", 0), max(0, len(sm) - 1))
+        sm, smax = sm[skip:], smax[skip:]
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
@@ -423,7 +441,23 @@ def run_ours(args, w):
     if st != fab.FA_OK:
         raise fab.FAError(st, "warm-up")
 
-    # ---- device-timed region: exactly K steps
+    # ---- device-timed region: exactly K steps, launched as one CUDA graph
+    # (the same kernels on the same data without the host's per-call work
+    # between them; plain launches if capture is unavailable)
+    graph = None
+    if not args.no_graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+                for _ in range(args.steps):
+                    step_fn()
+            with torch.cuda.stream(stream):
+                graph.replay()  # one untimed replay
+            torch.cuda.synchronize(dev)
+        except Exception as exc:  # noqa: BLE001 - report and time without the graph
+            print(f"bench: graph capture unavailable ({exc}); timing plain launches", file=sys.stderr)
+            graph = None
+            torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
@@ -432,10 +466,24 @@ def run_ours(args, w):
     with ClockSampler(local) as clocks:
         with torch.cuda.stream(stream):
             ev0.record(stream)
-            for _ in range(args.steps):
-                step()
+            if graph is not None:
+                graph.replay()
+                launches = args.steps * kernels_per_step
+            else:
+                for _ in range(args.steps):
+                    step()
             ev1.record(stream)
         torch.cuda.synchronize(dev)
+        # a region shorter than the sampling interval: keep the same load
+        # (untimed replays) until one more clock sample has landed
+        clock_window = "during the timed region"
+        if graph is not None and clocks.count() <= clocks.start_rows:
+            clock_window = "around the timed region (same graph replayed; region shorter than a sample)"
+            t_end = time.time() + 2.0
+            with torch.cuda.stream(stream):
+                while clocks.count() <= clocks.start_rows and time.time() < t_end:
+                    graph.replay()
+                    torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
     timed_launches = launches
@@ -515,13 +563,15 @@ def run_ours(args, w):
         "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": config_of(w, world, splits),
+        "config": dict(config_of(w, world, splits),
+                       launch="one CUDA graph of the K steps" if graph is not None else "K plain launches"),
         "frac_of_peak": frac_tensor,
         "roofline": roofline,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
         "gpu_launches": timed_launches,
-        "clocks": {k2: clk[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
+        "clocks": dict({k2: clk[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
+                       window=clock_window),
     }
     if world == 1 and not args.no_cpu_baseline:
         dout_np = I.make_dout(w.B, w.H, w.N, w.d, w.dtype, seed=wr.seed) if w.backward else None
@@ -543,6 +593,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=None, help="workload name (default: the headline shape)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time plain launches instead of a CUDA graph")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -302,7 +302,7 @@ __device__ __forceinline__ void zero_unloaded_q(uint8_t* q_tiles, int rows, int 
 // Round `n16` 16-byte groups of fp32 in shared memory to TF32 in place
 // (round to nearest, ties away), one warp.
 __device__ __forceinline__ void round_tf32_inplace(uint8_t* base, int n16, int lane) {
-#pragma unroll 1
+#pragma unroll 4
     for (int i = lane; i < n16; i += 32) {
         uint4* p4 = reinterpret_cast<uint4*>(base) + i;
         uint4 v = *p4;
@@ -322,7 +322,7 @@ __device__ __forceinline__ void round_tf32_inplace(uint8_t* base, int n16, int l
 template <int D>
 __device__ __forceinline__ void transpose_v_tf32(const uint8_t* vraw, uint8_t* vt, int lane) {
     constexpr int kDBlocks = D / 32;
-#pragma unroll 1
+#pragma unroll 4
     for (int i = 0; i < 32 * kDBlocks; ++i) {
         const int d = (i % kDBlocks) * 32 + lane;
         const int kg = i / kDBlocks;  // keys 4kg .. 4kg+3
