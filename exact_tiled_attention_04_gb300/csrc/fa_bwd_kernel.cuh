@@ -15,7 +15,9 @@
 //   warps 4-7  gradient warpgroup 1: query columns 64-127
 //   warp  8    tensor-core issuer (one thread) and TMEM owner
 //   warp  9    TMA producer (one thread)
-//   warps 10-11 idle (complete warpgroup 2 for the register reallocation)
+//   warp 10    dQ reducer (one thread): TMA tensor reductions of the
+//              staged dQ into the fp32 accumulator
+//   warp 11    idle (completes warpgroup 2 for the register reallocation)
 // Each thread of a gradient warpgroup owns one key row (its TMEM lane) and
 // half of the query columns.  The scores are computed transposed (keys on
 // the lanes) so that dK and dV accumulate in tensor memory for the whole

@@ -59,11 +59,11 @@ namespace fa {
 
 constexpr int kTileM = 128;  // query rows per softmax warpgroup = TMEM lanes
 constexpr int kTileN = 128;  // keys per K/V tile
-// Three warpgroups: two softmax warpgroups and one holding the tensor-core
-// issuer warp, the TMA warp and two idle warps.  Registers are allocated per
-// warpgroup, so the launch gets 384 x 168; setmaxnreg then moves them from
-// warpgroup 2 to the softmax warpgroups (per variant, see FwdCfg: the split
-// always sums to 384 x 168).
+// Three warpgroups: two softmax warpgroups and one holding the two
+// tensor-core issuer warps, the TMA warp and one idle warp.  Registers are
+// allocated per warpgroup, so the launch gets 384 x 168; setmaxnreg then
+// moves them from warpgroup 2 to the softmax warpgroups (per variant, see
+// FwdCfg: the split always sums to 384 x 168).
 constexpr int kThreads = 384;
 constexpr int kMmaWarp = 8;   // tensor-core issuer of query tile 0, TMEM owner
 constexpr int kMmaWarp2 = 10; // tensor-core issuer of query tile 1
@@ -522,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (skip) {
         // nothing issued: go straight to the teardown
     } else if (warp >= 8) {
-        // warpgroup 2: TMA producer, tensor-core issuer, two idle warps
+        // warpgroup 2: TMA producer, two tensor-core issuers, one idle warp
         regs_decrease<C::kOtherRegs>();
       if (!has_work) {
         // no visible key: nothing to load or multiply
