@@ -249,6 +249,22 @@ __device__ __forceinline__ void exp_half(const uint32_t (&s)[4][32], uint64_t c2
     }
 }
 
+// One unmasked half of P as 16-bit pairs into registers (for the
+// speculative path of the softmax loop; exp_half's arithmetic, no store).
+template <bool F16>
+__device__ __forceinline__ void exp_half_regs(const uint32_t (&s)[4][32], uint64_t c2, uint64_t ns2, int h,
+                                              uint32_t (&pw)[32], uint64_t (&acc)[4]) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int c0 = h * 64 + 2 * i;  // keys c0, c0 + 1
+        float t0, t1;
+        f2_unpack(f2_fma(f2_pack(u2f(s[c0 / 32][c0 % 32]), u2f(s[c0 / 32][c0 % 32 + 1])), c2, ns2), t0, t1);
+        const float p0 = ex2(t0), p1 = ex2(t1);
+        pw[i] = pack_16x2<F16>(p0, p1);
+        acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+    }
+}
+
 // Sum of the eight fp32 lanes of four packed pairs.
 __device__ __forceinline__ float sum8(const uint64_t (&a)[4]) {
     float x[8];
@@ -732,6 +748,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         if (q * 32 + i >= valid) s[q][i] = s[0][0];
+            }
+
+            // Speculation (16-bit inputs at d = 64, unmasked tiles after the
+            // first): the first half's exponentials against the current
+            // reference run while the row maximum reduces.  When no row of
+            // the warp moves its reference (the lazy threshold below), they
+            // are exactly the values the path below would compute and are
+            // published as they are; otherwise that path recomputes them.
+            // (d = 64: +5 to +8 %; d = 128: no gain, not used.)
+            if constexpr (!TF32 && D == 64) {
+                if (!masked && j > 0) {
+                    const float shift_s = (m_ref == -INFINITY) ? 0.0f : m_ref;
+                    const uint64_t c2s = f2_pack(c, c);
+                    const uint64_t ns2s = f2_pack(-shift_s, -shift_s);
+                    uint32_t pw0[32];
+                    uint64_t acc_s[4] = {0, 0, 0, 0};
+                    exp_half_regs<F16>(s, c2s, ns2s, 0, pw0, acc_s);
+                    const float mx_s = (c >= 0.0f) ? row_extreme<true>(s) : row_extreme<false>(s);
+                    const bool need_s = mx_s * c > m_ref + kRescaleThreshold;
+                    if (!__any_sync(0xffffffffu, need_s)) {
+                        tmem_st32(tS, pw0);
+                        tmem_st_wait();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(C::kBarPFull + 2 * w + 0));
+                        if (take_turns && C::kTurnAfterHalf == 0 && lane == 0) mbar_arrive(bar(C::kBarTurn + (1 - w)));
+                        exp_half<TF32, F16, false>(s, c2s, ns2s, valid, tS, 1, acc_s);
+                        tmem_st_wait();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(C::kBarPFull + 2 * w + 1));
+                        if (take_turns && C::kTurnAfterHalf == 1 && lane == 0) mbar_arrive(bar(C::kBarTurn + (1 - w)));
+                        const float tsum = sum8(acc_s);
+                        const float pmax = ex2(fmaf(mx_s, c, -shift_s));
+                        const float pmax_r = widen_lo16<F16>(pack_16x2<F16>(pmax, 0.0f));
+                        l += tsum;
+                        lq += tsum + (pmax_r - pmax);  // the exact path's order of operations
+                        continue;
+                    }
+                }
             }
 
             // tile maximum of t = s * c (c may be negative or zero)
