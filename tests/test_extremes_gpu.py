@@ -1,0 +1,82 @@
+"""Extreme sizes against the oracle on sampled outputs: very long sequences
+(forward N = 131072, backward N = 16384), very many short heads (4096 heads
+of 64 rows: one ragged tile each), and a decode step against a 262144-key
+cache with one key/value head for eight query heads (MQA)."""
+import numpy as np
+import pytest
+
+import oracle
+from exact_tiled_attention_04_gb300 import binding as fab
+from exact_tiled_attention_04_gb300 import inputs as I
+
+from .gpu_util import (TOL_LSE, compare_ex, ensure_library, grad_errors, run_bwd, run_fa_ex, tol_grad,
+                       tol_o_dtype)
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return ensure_library()
+
+
+def sample_rows(B, H, N, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = np.stack([rng.integers(0, B, n), rng.integers(0, H, n), rng.integers(0, N, n)], axis=1)
+    rows[:3] = [(0, 0, 0), (B - 1, H - 1, N - 1), (0, H - 1, N // 2)]
+    return rows
+
+
+@pytest.mark.parametrize("N,d", [(131072, 64), (65536, 128)])
+def test_forward_long_sequence(N, d):
+    q, k, v = I.make_general(1, 1, 1, N, N, d, "bf16", seed=800 + d)
+    for causal in (False, True):
+        o, lse = run_fa_ex(q, k, v, "bf16", 1, causal=causal)
+        rows = sample_rows(1, 1, N, 12, 801)
+        err_o, err_l = compare_ex("bf16", o, lse, q, k, v, rows=rows, causal=causal)
+        assert err_o <= tol_o_dtype("bf16") and err_l <= TOL_LSE, (causal, err_o, err_l)
+
+
+def test_forward_many_short_heads():
+    q, k, v = I.make_general(64, 64, 64, 64, 64, 64, "bf16", seed=810)
+    o, lse = run_fa_ex(q, k, v, "bf16", 1)
+    rows = sample_rows(64, 64, 64, 64, 811)
+    err_o, err_l = compare_ex("bf16", o, lse, q, k, v, rows=rows)
+    assert err_o <= tol_o_dtype("bf16") and err_l <= TOL_LSE
+
+
+def test_decode_long_cache_mqa():
+    B, H, H_kv, Nkv, d = 2, 8, 1, 262144, 128
+    q, k, v = I.make_general(B, H, H_kv, 1, Nkv, d, "bf16", seed=820)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    splits = fab.fa_fwd_ex_splits(B, H, H_kv, 1, Nkv, sms)
+    o, lse = run_fa_ex(q, k, v, "bf16", splits)
+    err_o, err_l = compare_ex("bf16", o, lse, q, k, v)
+    assert err_o <= tol_o_dtype("bf16") and err_l <= TOL_LSE, (splits, err_o, err_l)
+
+
+def test_backward_long_sequence():
+    B, H, N, d = 1, 1, 16384, 128
+    q, k, v = I.make_general(B, H, H, N, N, d, "bf16", seed=830, factor=0.5)
+    dout = I.make_dout(B, H, N, d, "bf16", seed=830)
+    (dq, dk, dv), sc = run_bwd(q, k, v, dout, "bf16")
+    rows = sample_rows(B, H, N, 8, 831)
+    ref_dq = oracle.attention_bwd_dq_rows_f64(q, k, v, dout, sc, rows)
+    e_dq = np.max(np.abs(dq[rows[:, 0], rows[:, 1], rows[:, 2]] - ref_dq)) / np.max(np.abs(ref_dq))
+    cols = np.array([(0, 0, 0), (0, 0, 8191), (0, 0, N - 1)])
+    ref_dk, ref_dv = oracle.attention_bwd_dkv_cols_f64(q, k, v, dout, sc, cols)
+    got = [g[cols[:, 0], cols[:, 1], cols[:, 2]] for g in (dk, dv)]
+    e_dk = np.max(np.abs(got[0] - ref_dk)) / np.max(np.abs(ref_dk))
+    e_dv = np.max(np.abs(got[1] - ref_dv)) / np.max(np.abs(ref_dv))
+    assert max(e_dq, e_dk, e_dv) <= tol_grad("bf16"), (e_dq, e_dk, e_dv)
+
+
+def test_backward_many_short_heads():
+    q, k, v = I.make_general(16, 64, 16, 64, 100, 64, "bf16", seed=840)
+    dout = I.make_dout(16, 64, 64, 64, "bf16", seed=840)
+    got, sc = run_bwd(q, k, v, dout, "bf16", causal=True)
+    errs = grad_errors(got, oracle.attention_bwd_f64(q, k, v, dout, sc, causal=True))
+    assert max(errs) <= tol_grad("bf16"), errs
