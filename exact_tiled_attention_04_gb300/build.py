@@ -25,7 +25,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 SOURCES = ["fa_api.cu", "fa_fwd_bf16.cu", "fa_fwd_f16.cu", "fa_fwd_tf32.cu", "fa_merge.cu",
-           "fa_bwd_api.cu", "fa_bwd_bf16.cu", "fa_bwd_f16.cu", "fa_bwd_aux.cu", "fa_pipeline.cu"]
+           "fa_bwd_api.cu", "fa_bwd_bf16.cu", "fa_bwd_f16.cu", "fa_bwd_aux.cu", "fa_pipeline.cu",
+           "fa_dec_bf16.cu", "fa_dec_f16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -174,10 +174,17 @@ bool packed_heads(int64_t H, int64_t H_kv, int64_t N_q) {
     return group > 1 && N_q * group <= 128;
 }
 
+// Decode steps: at most 32 query rows per key/value head (N_q x group) go to
+// the decode kernel (16-bit inputs), one CTA per key/value head and key
+// partition, keys on the tensor-memory lanes.
+constexpr int64_t kDecodeMaxRows = 32;
+bool decode_rows(int64_t H, int64_t H_kv, int64_t N_q) { return N_q * (H / H_kv) <= kDecodeMaxRows; }
+
 // CTAs of one key partition: query blocks of 256 rows per head (per key/value
-// head when packed).
+// head when packed or in the decode kernel; with group 1 and N_q <= 32 the
+// two counts agree, so the count does not depend on the dtype).
 int64_t ctas_per_partition(int64_t B, int64_t H, int64_t H_kv, int64_t N_q) {
-    if (packed_heads(H, H_kv, N_q)) return B * H_kv;
+    if (packed_heads(H, H_kv, N_q) || decode_rows(H, H_kv, N_q)) return B * H_kv;
     return B * H * ((N_q + 255) / 256);
 }
 constexpr int kMaxSplits = 32;  // the merge kernel holds one partition per lane
@@ -260,8 +267,9 @@ int launch_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     const int64_t BH = B * H;
     const SplitPlan sp = plan_splits(N_kv, num_splits);
     const bool pack = packed_heads(H, H_kv, N_q);
-    const uint32_t qbox_rows = pack ? static_cast<uint32_t>(N_q) : 128u;
-    const uint32_t qbox_heads = pack ? static_cast<uint32_t>(H / H_kv) : 1u;
+    const bool dec = dtype != FA_DTYPE_F32 && decode_rows(H, H_kv, N_q);
+    const uint32_t qbox_rows = (pack || dec) ? static_cast<uint32_t>(N_q) : 128u;
+    const uint32_t qbox_heads = (pack || dec) ? static_cast<uint32_t>(H / H_kv) : 1u;
     CUtensorMap mq, mk, mv, mo;
     int st;
     if ((st = encode_map(&mq, q, dtype, BH, N_q, d, qbox_rows, qbox_heads)) != FA_OK) return st;
@@ -297,8 +305,13 @@ int launch_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     const unsigned int grid = static_cast<unsigned int>(ctas_per_partition(B, H, H_kv, N_q) * sp.splits);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
+    p.out = o;
     cudaError_t e;
-    if (dtype == FA_DTYPE_BF16 && d == 64)
+    if (dec && dtype == FA_DTYPE_BF16)
+        e = fa::launch_decode_bf16(static_cast<int>(d), mq, mk, mv, p, grid, s);
+    else if (dec)
+        e = fa::launch_decode_f16(static_cast<int>(d), mq, mk, mv, p, grid, s);
+    else if (dtype == FA_DTYPE_BF16 && d == 64)
         e = fa::launch_fwd_bf16_d64(mq, mk, mv, mo, p, grid, s);
     else if (dtype == FA_DTYPE_BF16)
         e = fa::launch_fwd_bf16_d128(mq, mk, mv, mo, p, grid, s);

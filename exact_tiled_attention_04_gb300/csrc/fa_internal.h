@@ -41,6 +41,7 @@ struct FwdParams {
     // splits > 1: unnormalised partial results, one slab per partition
     float* o_part;           // fp32 [splits, B*H, Nq, d]
     float* ml_part;          // fp32 [splits, B*H, Nq, 4]: m (base 2, scaled), l, lq, unused
+    void* out;               // decode kernel, splits == 1: O [B*H, Nq, d] (input dtype)
 };
 
 // Merge of split partial results: O = sum_s w_s O_s / sum_s w_s lq_s,
@@ -85,5 +86,14 @@ cudaError_t launch_fwd_f16_d128(const CUtensorMap& q, const CUtensorMap& k, cons
 cudaError_t launch_fwd_tf32_d64(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                                 const CUtensorMap& o, const FwdParams& p, unsigned int grid,
                                 cudaStream_t stream);
+
+// Decode kernel (fa_decode_kernel.cuh): rows Nq * group <= 32 per key/value
+// head, one CTA per (batch, key/value head) and key partition: grid =
+// B * H_kv * p.splits.  q over [B*H, Nq, d] with boxes of Nq rows x group
+// heads; k, v over [B*H_kv, Nkv, d].  d is 64 or 128.
+cudaError_t launch_decode_bf16(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                               const FwdParams& p, unsigned int grid, cudaStream_t stream);
+cudaError_t launch_decode_f16(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                              const FwdParams& p, unsigned int grid, cudaStream_t stream);
 
 }  // namespace fa
