@@ -104,13 +104,13 @@ SHARED_SOURCES = ("fa_ptx.cuh", "fa_internal.h", "fa_host.h")
 def kernel_source_hash(backward: bool = False) -> str:
     """Hash of the CUDA sources a pass's kernels and launches are built from:
     ties a stored ncu traffic figure to the kernel it was measured on.
-    Forward: fa_fwd*, fa_merge*, fa_api.cu; backward: fa_bwd*; both: the
-    headers they share."""
+    Forward: fa_fwd*, fa_dec*, fa_decode*, fa_merge*, fa_api.cu; backward:
+    fa_bwd*; both: the headers they share."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_tiled_attention_04_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         mine = (name.startswith("fa_bwd") if backward
-                else name.startswith(("fa_fwd", "fa_merge")) or name == "fa_api.cu")
+                else name.startswith(("fa_fwd", "fa_dec", "fa_merge")) or name == "fa_api.cu")
         if mine or name in SHARED_SOURCES:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
@@ -541,7 +541,11 @@ def run_ours(args, w):
         kernel_name = (f"fa_bwd_kernel<{w.dtype},{w.d}{',causal' if w.causal else ''}> + fa_bwd_prep_kernel"
                        " + fa_bwd_dq_kernel (timed as the whole step)")
     else:
-        kernel_name = (f"fa_fwd_kernel<{w.dtype},{w.d}{',causal' if w.causal else ''}>"
+        # the decode kernel takes 16-bit inputs with at most 32 query rows per
+        # key/value head (N x H / H_kv), like the library's own dispatch
+        decode = w.dtype != "f32" and w.N * (w.H // w.H_kv) <= 32
+        kernel_name = (f"{'fa_decode_kernel' if decode else 'fa_fwd_kernel'}"
+                       f"<{w.dtype},{w.d}{',causal' if w.causal else ''}>"
                        + (" + fa_merge_kernel" if kernels_per_step == 2 else ""))
     if intensity >= ridge:
         achieved = w.flops() / step_s / 1e12

@@ -102,13 +102,29 @@ struct FwdCfg {
     static constexpr int kPvSplit = 1;
     static constexpr uint32_t kIdescPV = instr_desc(kFmt, false, !TF32, kTileM, kPvN);
 
-    // The other softmax warpgroup may start once this one has published
-    // half kTurnAfterHalf of P.  d = 128: after the whole tile (strict
-    // alternation keeps the tensor core fed); d = 64: after the first half
-    // (the products are short, the exponentials dominate, so overlapping the
-    // two warpgroups' exponentials wins; measured +7 % at d = 64, -7 % at
-    // d = 128).
+    // Where the two softmax warpgroups take turns (kTakeTurns), the other
+    // one may start once this one has published half kTurnAfterHalf of P.
+    // d = 128: after the whole tile (strict alternation keeps the tensor
+    // core fed); fp32 inputs at d = 64: after the first half (overlapping
+    // the two warpgroups' exponentials wins there; measured +7 % at d = 64,
+    // -7 % at d = 128).
     static constexpr int kTurnAfterHalf = (D == 64) ? 0 : 1;
+
+    // Early scores (16-bit inputs at d = 64, where the four tiles of S, P
+    // and O fit the 512 TMEM columns side by side): P has columns of its
+    // own, so S(j+1) = Q K_{j+1}^T is enqueued as soon as the softmax has
+    // read S(j) into registers, ahead of O += P(j) V.  The next tile's
+    // scores are then ready when the softmax finishes a tile, instead of a
+    // product's latency later.  Elsewhere P overwrites S (d = 128 needs
+    // the columns) and S(j+1) follows O += P(j) V.
+    static constexpr bool kEarlyS = !TF32 && D == 64;
+    static constexpr uint32_t kColP = 256;                  // kEarlyS: P_w at 256 + 64 w
+    static constexpr uint32_t kColO = kEarlyS ? 384 : 256;  // O_w at kColO + D w
+    // With early scores each warpgroup's next tile is ready when it needs
+    // it, and turns would only serialise the two softmaxes: they run freely
+    // (measured at d = 64: early scores alone +4 %, and without turns
+    // +24 % on top).
+    static constexpr bool kTakeTurns = !kEarlyS;
 
     // register split (setmaxnreg): softmax warpgroups / warpgroup 2, chosen
     // so that neither side spills
@@ -138,18 +154,17 @@ struct FwdCfg {
     static constexpr int kBarKRaw = kBarQRaw + 1;   // [kKStages]
     static constexpr int kBarVRaw = kBarKRaw + kKStages;
     static constexpr int kBarTurn = kBarVRaw + 1;  // [2]: softmax warpgroup w may start a tile
-    static constexpr int kNumBars = kBarTurn + 2;
+    static constexpr int kBarSFree = kBarTurn + 2;   // [2] kEarlyS: S_w read (4 warps)
+    static constexpr int kBarPVDone = kBarSFree + 2; // [2] kEarlyS: O_w += P_w V done
+    static constexpr int kNumBars = kBarPVDone + 2;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kSmemUsed = kOffAbort + 4;
     static constexpr size_t kSmemBytes = static_cast<size_t>(kSmemUsed) + 1024;  // alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
-    static_assert(256 + 2 * D <= static_cast<int>(kTmemCols), "tensor memory budget exceeded");
+    static_assert(kColO + 2 * D <= kTmemCols, "tensor memory budget exceeded");
 };
 
-// Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting
-// (if `honor_abort`) or when this wait itself gave up after kWaitLimitNs, in
-// which case it raises the abort flag and the device error word.
 // Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting
 // (if `honor_abort`) or when this wait itself gave up after kWaitLimitNs, in
 // which case it raises the CTA's abort flag, sets the sticky device error
@@ -508,6 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(C::kBarPFull + 2 * w + 0), 4);  // one arrival per softmax warp
             mbar_init(bar(C::kBarPFull + 2 * w + 1), 4);
             mbar_init(bar(C::kBarTurn + w), 4);
+            mbar_init(bar(C::kBarSFree + w), 4);
+            mbar_init(bar(C::kBarPVDone + w), 1);
             mbar_init(bar(C::kBarOFull + w), 1);
             mbar_init(bar(C::kBarEpi + w), kTileM);
         }
@@ -607,7 +624,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && !(one_tile && warp == kMmaWarp2)) {
             const int w = (warp == kMmaWarp) ? 0 : 1;
             const uint32_t dS = tmem + 128u * static_cast<uint32_t>(w);
-            const uint32_t dO = tmem + 256u + static_cast<uint32_t>(D * w);
+            const uint32_t dO = tmem + C::kColO + static_cast<uint32_t>(D * w);
+            // P_w: over S_w, or its own columns (kEarlyS)
+            const uint32_t dP = C::kEarlyS ? tmem + C::kColP + 64u * static_cast<uint32_t>(w) : dS;
             const uint32_t sQ = sbase + C::kOffQ + w * C::kTileBytes;
             auto issue_qk = [&](int ks) {
                 const uint32_t sK = sbase + C::kOffK + ks * C::kTileBytes;
@@ -633,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // kAtomBytes apart; a k-step is 16 rows
                         db = smem_desc_sw128(sV + kk * C::kUmmaK * 128, C::kAtomBytes, 1024);
                     }
-                    mma_ts<TF32>(dO, dS + kk * 8, db, C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+                    mma_ts<TF32>(dO, dP + kk * 8, db, C::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
                 }
             };
 
@@ -648,6 +667,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; ok && j < T; ++j) {
                 const int vs = j % C::kVStages;
                 const int ks = (j + 1) % C::kKStages;
+                if (C::kEarlyS && j + 1 < T) {
+                    // S(j+1) as soon as the softmax has read S(j)
+                    ok = wait_phase(bar(C::kBarSFree + w), j & 1, abort_flag, p, 14);
+                    if (!ok) break;
+                    ok = wait_phase(bar(C::kBarKFull + ks), ((j + 1) / C::kKStages) & 1, abort_flag, p, 7);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_qk(ks);
+                    tc_commit(bar(C::kBarSFull + w));
+                    tc_commit(bar(C::kBarKEmpty + ks));
+                }
                 ok = wait_phase(bar(C::kBarVFull + vs), (j / C::kVStages) & 1, abort_flag, p, 5);
                 if (!ok) break;
                 // the first half of P (keys 0-63) is published before the
@@ -661,7 +691,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 issue_pv(vs, true, C::kPvSteps / 2, C::kPvSteps);
                 tc_commit(bar(C::kBarVEmpty + vs));
-                if (j + 1 < T) {
+                if (C::kEarlyS) {
+                    tc_commit(bar(C::kBarPVDone + w));
+                    if (j + 1 == T) tc_commit(bar(C::kBarOFull + w));
+                } else if (j + 1 < T) {
                     ok = wait_phase(bar(C::kBarKFull + ks), ((j + 1) / C::kKStages) & 1, abort_flag, p, 7);
                     if (!ok) break;
                     tc_fence_after();
@@ -686,10 +719,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = wi * 32 + lane;  // row within the tile = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(wi * 32) << 16;
         const uint32_t tS = tmem + lane_off + 128u * static_cast<uint32_t>(w);
-        const uint32_t tO = tmem + lane_off + 256u + static_cast<uint32_t>(D * w);
+        const uint32_t tO = tmem + lane_off + C::kColO + static_cast<uint32_t>(D * w);
+        // where this warp writes P: over its scores, or P_w's own columns (kEarlyS)
+        const uint32_t tP = C::kEarlyS ? tmem + lane_off + C::kColP + 64u * static_cast<uint32_t>(w) : tS;
         const float c = p.scale_log2;
         const bool active = !(one_tile && w == 1);  // this warpgroup's tile has rows
-        const bool take_turns = !one_tile;
+        const bool take_turns = C::kTakeTurns && !one_tile;
 
         // keys of this row's head visible to this row: all Nkv, or under the
         // causal mask those up to i + causal_offset (may be none)
@@ -713,9 +748,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   // tile's largest weight as rounded for P V
         bool ok = true;
 
-        // The two softmax warpgroups take turns (0, 1, 0, 1, ...): one runs its
-        // exponentials while the other tile's products occupy the tensor core
-        // (see kTurnAfterHalf for how far the turns overlap).
+        // Where they take turns (kTakeTurns), the two softmax warpgroups go
+        // 0, 1, 0, 1, ...: one runs its exponentials while the other tile's
+        // products occupy the tensor core (see kTurnAfterHalf for how far the
+        // turns overlap).
         if (take_turns && w == 1 && lane == 0) mbar_arrive(bar(C::kBarTurn + 0));
         const int T_rows = active ? T : 0;
         for (int j = 0; j < T_rows; ++j) {  // T <= 0: no key tile
@@ -734,6 +770,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < 4; ++q) tmem_ld32(tS + 32u * q, s[q]);
 #pragma unroll
             for (int q = 0; q < 4; ++q) tmem_ld_wait(s[q]);
+            if constexpr (C::kEarlyS) {
+                // S_w may be overwritten by the next tile's scores
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::kBarSFree + w));
+            }
+            // kEarlyS: P_w and O_w hold tile j-1's product until it completes
+            // (that product is not ordered before this tile's scores)
+            auto wait_prev_product = [&]() -> bool {
+                if (!C::kEarlyS || j == 0) return true;
+                return __all_sync(0xffffffffu, wait_phase(bar(C::kBarPVDone + w), (j - 1) & 1, abort_flag, p, 15));
+            };
 
             // keys of this tile visible to this row (<= 0: none, >= 128: all);
             // masking is decided per warp (tcgen05.st is warp-collective)
@@ -768,13 +816,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float mx_s = (c >= 0.0f) ? row_extreme<true>(s) : row_extreme<false>(s);
                     const bool need_s = mx_s * c > m_ref + kRescaleThreshold;
                     if (!__any_sync(0xffffffffu, need_s)) {
-                        tmem_st32(tS, pw0);
+                        if (!wait_prev_product()) {
+                            ok = false;
+                            break;
+                        }
+                        tmem_st32(tP, pw0);
                         tmem_st_wait();
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar(C::kBarPFull + 2 * w + 0));
                         if (take_turns && C::kTurnAfterHalf == 0 && lane == 0) mbar_arrive(bar(C::kBarTurn + (1 - w)));
-                        exp_half<TF32, F16, false>(s, c2s, ns2s, valid, tS, 1, acc_s);
+                        exp_half<TF32, F16, false>(s, c2s, ns2s, valid, tP, 1, acc_s);
                         tmem_st_wait();
                         tc_fence_before();
                         __syncwarp();
@@ -807,8 +859,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             if (j > 0 && __any_sync(0xffffffffu, need)) {
                 // O holds the previous tiles' contributions (their products
-                // completed before this tile's scores were signalled); the
-                // next product into O waits for this warp's first arrival.
+                // completed before this tile's scores were signalled, or, with
+                // kEarlyS, once the last one signals); the next product into
+                // O waits for this warp's first arrival.
+                if (!wait_prev_product()) {
+                    ok = false;
+                    break;
+                }
 #pragma unroll
                 for (int q = 0; q < D / 32; ++q) {
                     uint32_t o[32];
@@ -832,12 +889,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t c2 = f2_pack(c, c);
             const uint64_t ns2 = f2_pack(-shift, -shift);
             uint64_t acc[4] = {0, 0, 0, 0};
+            if (!wait_prev_product()) {
+                ok = false;
+                break;
+            }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 if (masked) {
-                    exp_half<TF32, F16, true>(s, c2, ns2, valid, tS, h, acc);
+                    exp_half<TF32, F16, true>(s, c2, ns2, valid, tP, h, acc);
                 } else {
-                    exp_half<TF32, F16, false>(s, c2, ns2, valid, tS, h, acc);
+                    exp_half<TF32, F16, false>(s, c2, ns2, valid, tP, h, acc);
                 }
                 tmem_st_wait();
                 tc_fence_before();
