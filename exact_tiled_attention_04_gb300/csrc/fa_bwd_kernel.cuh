@@ -229,9 +229,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     const int warp = static_cast<int>(threadIdx.x) / 32;
     const int lane = static_cast<int>(threadIdx.x) % 32;
-    // blockIdx.x = unit * n_kv_blocks + kb, unit = b * H_kv + key/value head
-    const int kb = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.n_kv_blocks));
-    const int unit = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.n_kv_blocks));
+    // unit = b * H_kv + key/value head; kb = key block of the unit.  Causal:
+    // key block 0 sees every query tile and later blocks fewer, so they go
+    // heaviest first, by groups of units; otherwise blockIdx.x = unit *
+    // n_kv_blocks + kb.
+    int kb, unit;
+    if (kCausal) {
+        lpt_item(blockIdx.x, static_cast<int>(gridDim.x) / p.n_kv_blocks, p.n_kv_blocks, unit, kb);
+    } else {
+        kb = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.n_kv_blocks));
+        unit = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.n_kv_blocks));
+    }
     const int b = unit / p.H_kv;
     const int kvh = unit % p.H_kv;
     // Query tiles that see a key of this block: all, or under the causal mask

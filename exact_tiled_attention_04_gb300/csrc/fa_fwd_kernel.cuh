@@ -469,15 +469,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = static_cast<int>(threadIdx.x) / 32;
     const int lane = static_cast<int>(threadIdx.x) % 32;
-    // blockIdx.x = ((bh * n_q_blocks) + qb) * splits + split
+    // blockIdx.x = cta * splits + split; cta = bh * n_q_blocks + qb, or
+    // (causal) the heavy-first order of lpt_item over (bh, block)
     // grouped heads packed into query tile 0 (p.pack; always set when kOneTile)
     const bool pack = kOneTile || p.pack != 0;
     const unsigned int split = blockIdx.x % static_cast<unsigned>(p.splits);
     const unsigned int cta = blockIdx.x / static_cast<unsigned>(p.splits);
-    // causal: later query blocks see more keys; they are launched first
-    const int qb_lin = static_cast<int>(cta % static_cast<unsigned>(p.n_q_blocks));
-    const int qb = kCausal ? p.n_q_blocks - 1 - qb_lin : qb_lin;
-    const int bh = static_cast<int>(cta / static_cast<unsigned>(p.n_q_blocks));
+    int qb, bh;
+    if (kCausal) {
+        // later query blocks see more keys: heaviest first, by groups of heads
+        // (packed launches have one block per key/value head)
+        const int units = static_cast<int>(gridDim.x / static_cast<unsigned>(p.splits)) / p.n_q_blocks;
+        int rank;
+        lpt_item(cta, units, p.n_q_blocks, bh, rank);
+        qb = p.n_q_blocks - 1 - rank;
+    } else {
+        qb = static_cast<int>(cta % static_cast<unsigned>(p.n_q_blocks));
+        bh = static_cast<int>(cta / static_cast<unsigned>(p.n_q_blocks));
+    }
     // key/value head of this query head (grouped-query attention: H / H_kv
     // query heads share one key/value head)
     // packed: bh is the key/value head itself; otherwise its query head's

@@ -335,4 +335,26 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthread
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Launch order of work items (unit, rank) for grids whose items have uneven
+// cost (causal masks: rank 0 is the heaviest item of each unit, cost falling
+// with rank).  Units go in groups; within a group every unit's rank 0 comes
+// first, then every rank 1, and so on, so the heavy items of the last units
+// do not start at the end of the grid, while the CTAs in flight still share
+// the operands of a few units in L2.  A group holds at least 8 units and at
+// least 128 items (measured on causal launches against heaviest-first within
+// each unit alone: +6.5 % forward and +2.4 % backward at d = 128, +10 to
+// +20 % at d = 64; groups of 4 or 16 units did no better overall).  `i`
+// runs over units * per_unit items.
+__device__ __forceinline__ void lpt_item(unsigned int i, int units, int per_unit, int& unit, int& rank) {
+    int group = (128 + per_unit - 1) / per_unit;
+    group = group < 8 ? 8 : (group > 64 ? 64 : group);
+    const unsigned int group_items = static_cast<unsigned>(group) * static_cast<unsigned>(per_unit);
+    const int g = static_cast<int>(i / group_items);
+    const int first = g * group;                                   // first unit of the group
+    const int gs = units - first < group ? units - first : group;  // units in this group
+    const int j = static_cast<int>(i - static_cast<unsigned>(g) * group_items);
+    rank = j / gs;
+    unit = first + j % gs;
+}
+
 }  // namespace fa
