@@ -35,11 +35,16 @@ size_t workspace_bytes(int64_t B, int64_t H, int64_t N_q, int64_t d) {
 
 bool misaligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
-int validate_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                 const float* lse, const void* dq, const void* dk, const void* dv, int64_t B, int64_t H,
-                 int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d, float scale, int dtype_arg,
-                 const void* workspace, size_t workspace_bytes_given) {
-    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
+}  // namespace
+
+namespace fa {
+// The argument checks of fa_bwd that concern the tensors: sizes, dtype, flags,
+// alignment and overlaps (the outputs dq, dk, dv overlap no input and no other
+// output).  The workspace is checked by the caller.
+int validate_bwd_tensors(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                         const float* lse, const void* dq, const void* dk, const void* dv, int64_t B, int64_t H,
+                         int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d, float scale, int dtype_arg) {
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || H_kv < 1 || N_q < 1 || N_kv < 1 || d < 1) return FA_ERR_INVALID_ARG;
     if (H % H_kv != 0) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
@@ -57,25 +62,59 @@ int validate_bwd(const void* q, const void* k, const void* v, const void* o, con
     if (BH > kInt32Max || N_q > kInt32Max - 128 || N_kv > kInt32Max - 128) return FA_ERR_UNSUPPORTED;
     if (BHkv > kInt32Max / ((N_kv + 127) / 128)) return FA_ERR_UNSUPPORTED;
     if (misaligned16(q) || misaligned16(k) || misaligned16(v) || misaligned16(o) || misaligned16(dout) ||
-        misaligned16(dq) || misaligned16(dk) || misaligned16(dv) || misaligned16(workspace))
+        misaligned16(dq) || misaligned16(dk) || misaligned16(dv))
         return FA_ERR_ALIGNMENT;
     if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_ALIGNMENT;
-    const size_t need = workspace_bytes(B, H, N_q, d);
-    if (workspace_bytes_given < need) return FA_ERR_INVALID_ARG;
-    // outputs (dq, dk, dv, workspace) overlap no input and no other output
-    const size_t qbytes = static_cast<size_t>(BH * N_q * d * 2);
-    const size_t kvbytes = static_cast<size_t>(BHkv * N_kv * d * 2);
-    const size_t lbytes = static_cast<size_t>(BH * N_q) * sizeof(float);
     const void* in_ptr[6] = {q, k, v, o, dout, lse};
-    const size_t in_len[6] = {qbytes, kvbytes, kvbytes, qbytes, qbytes, lbytes};
-    const void* out_ptr[4] = {dq, dk, dv, workspace};
-    const size_t out_len[4] = {qbytes, kvbytes, kvbytes, need};
-    for (int a = 0; a < 4; ++a) {
+    size_t in_len[6];
+    bwd_tensor_bytes(B, H, H_kv, N_q, N_kv, d, in_len);
+    const void* out_ptr[3] = {dq, dk, dv};
+    const size_t out_len[3] = {in_len[0], in_len[1], in_len[2]};
+    for (int a = 0; a < 3; ++a) {
         for (int i = 0; i < 6; ++i)
             if (overlaps(out_ptr[a], out_len[a], in_ptr[i], in_len[i])) return FA_ERR_INVALID_ARG;
-        for (int b2 = a + 1; b2 < 4; ++b2)
+        for (int b2 = a + 1; b2 < 3; ++b2)
             if (overlaps(out_ptr[a], out_len[a], out_ptr[b2], out_len[b2])) return FA_ERR_INVALID_ARG;
     }
+    return FA_OK;
+}
+
+// Bytes of q, k, v, o, dout, lse (in that order; dq, dk, dv are the sizes of
+// q, k, v) for 16-bit inputs.
+void bwd_tensor_bytes(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d, size_t* len) {
+    const size_t qbytes = static_cast<size_t>(B * H * N_q * d * 2);
+    const size_t kvbytes = static_cast<size_t>(B * H_kv * N_kv * d * 2);
+    len[0] = qbytes;
+    len[1] = kvbytes;
+    len[2] = kvbytes;
+    len[3] = qbytes;
+    len[4] = qbytes;
+    len[5] = static_cast<size_t>(B * H * N_q) * sizeof(float);
+}
+}  // namespace fa
+
+namespace {
+
+int validate_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, const void* dq, const void* dk, const void* dv, int64_t B, int64_t H,
+                 int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d, float scale, int dtype_arg,
+                 const void* workspace, size_t workspace_bytes_given) {
+    if (!workspace) return FA_ERR_INVALID_ARG;
+    const int st = fa::validate_bwd_tensors(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, N_q, N_kv, d, scale,
+                                            dtype_arg);
+    if (st != FA_OK) return st;
+    if (misaligned16(workspace)) return FA_ERR_ALIGNMENT;
+    const size_t need = workspace_bytes(B, H, N_q, d);
+    if (workspace_bytes_given < need) return FA_ERR_INVALID_ARG;
+    // the workspace overlaps no input and no output
+    const void* ptr[9] = {q, k, v, o, dout, lse, dq, dk, dv};
+    size_t len[9];
+    fa::bwd_tensor_bytes(B, H, H_kv, N_q, N_kv, d, len);
+    len[6] = len[0];
+    len[7] = len[1];
+    len[8] = len[2];
+    for (int i = 0; i < 9; ++i)
+        if (overlaps(workspace, need, ptr[i], len[i])) return FA_ERR_INVALID_ARG;
     return FA_OK;
 }
 

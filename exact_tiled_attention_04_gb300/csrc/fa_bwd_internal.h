@@ -65,6 +65,15 @@ struct BwdDqParams {
     float scale;
 };
 
+// Host-side argument checks of fa_bwd on the tensors alone (sizes, dtype,
+// flags, alignment, and that dq, dk, dv overlap no input and no other
+// output); returns an FA_* status.  The workspace is the caller's to check.
+int validate_bwd_tensors(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                         const float* lse, const void* dq, const void* dk, const void* dv, int64_t B, int64_t H,
+                         int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d, float scale, int dtype_arg);
+// Bytes of q, k, v, o, dout, lse (16-bit inputs) into len[0..5].
+void bwd_tensor_bytes(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d, size_t* len);
+
 cudaError_t launch_bwd_prep(const BwdPrepParams& p, int d, int dtype, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const BwdDqParams& p, int dtype, cudaStream_t stream);
 

@@ -194,3 +194,33 @@ def test_host_pipeline_validation(lib):
     assert fab.fa_fwd_host(*args, WS + 16, need, None) == fab.FA_ERR_ALIGNMENT
     assert fab.fa_fwd_host(Q, K, V, O, L, 2, 8, 2, 300, 300, 96, 0.088, code, WS, need, None) == \
         fab.FA_ERR_UNSUPPORTED
+
+
+def test_host_pipeline_workspace_is_checked_with_its_own_size(lib):
+    """The host pipelines check their device workspace with the size they
+    need, not the (larger) workspace of the device entry point on the whole
+    problem: a tensor placed right after the pipeline workspace is accepted,
+    one that reaches into it is rejected."""
+    B, H, N, d = 2, 32, 8192, 128
+    code = fab.FA_DTYPE_BF16
+    need = fab.fa_bwd_host_workspace_size(B, H, H, N, N, d)
+    assert 0 < need < fab.fa_bwd_workspace_size(B, H, N, d)
+    qb = B * H * N * d * 2
+    lb = B * H * N * 4
+    ws = 1 << 40
+    # q, k, v, o, dout, lse, dq, dk, dv one after another, the first one
+    # `start` bytes after the workspace
+    def ptrs(start):
+        sizes = [qb] * 5 + [lb] + [qb] * 3
+        out, a = [], ws + start
+        for sz in sizes:
+            out.append(a)
+            a += (sz + 255) // 256 * 256
+        return out
+    overlapping = ptrs(need - 256)
+    assert fab.fa_bwd_host(*overlapping, B, H, H, N, N, d, 0.088, code, ws, need, None) == fab.FA_ERR_INVALID_ARG
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("the accepted case would run the pipeline on fake host pointers")
+    adjacent = ptrs(need)
+    assert fab.fa_bwd_host(*adjacent, B, H, H, N, N, d, 0.088, code, ws, need, None) == fab.FA_ERR_CUDA

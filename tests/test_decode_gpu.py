@@ -87,3 +87,11 @@ def test_matches_grouped_tile_path_closely():
     o32, l32 = run_fa_ex(q[:, :32], k, v, "bf16", 1)
     assert np.max(np.abs(o33[:, :32] - o32)) <= 2 ** -7
     assert np.max(np.abs(l33[:, :32] - l32)) <= 1e-4
+
+
+@pytest.mark.parametrize("splits", [1, 2])
+def test_fp16_causal_32_rows(splits):
+    """fp16, causal, the 32-row variant at d = 128 (four queries of eight
+    query heads per key/value head)."""
+    q, k, v = I.make_general(1, 16, 2, 4, 500, 128, "f16", seed=970 + splits)
+    check("f16", q, k, v, splits, causal=True)

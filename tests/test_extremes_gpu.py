@@ -80,3 +80,39 @@ def test_backward_many_short_heads():
     got, sc = run_bwd(q, k, v, dout, "bf16", causal=True)
     errs = grad_errors(got, oracle.attention_bwd_f64(q, k, v, dout, sc, causal=True))
     assert max(errs) <= tol_grad("bf16"), errs
+
+
+def test_causal_forward_item_order_groups():
+    """Causal forward blocks are launched heaviest first within groups of
+    heads (8 heads of 16 blocks each here, then a partial group of 3): every
+    output row is written (the outputs start as NaN) and sampled rows of
+    every head match the oracle."""
+    B, H, N, d = 1, 11, 4096, 64
+    q, k, v = I.make_general(B, H, H, N, N, d, "bf16", seed=850)
+    o, lse = run_fa_ex(q, k, v, "bf16", 1, causal=True)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    rng = np.random.default_rng(851)
+    rows = np.array([(0, h, i) for h in range(H) for i in (0, 255, 256, N - 1, int(rng.integers(0, N)))])
+    err_o, err_l = compare_ex("bf16", o, lse, q, k, v, rows=rows, causal=True)
+    assert err_o <= tol_o_dtype("bf16") and err_l <= TOL_LSE, (err_o, err_l)
+
+
+def test_causal_backward_item_order_groups():
+    """Causal backward key blocks are launched heaviest first within groups
+    of key/value heads (8 heads of 32 blocks, then 3; two query heads per
+    key/value head): every gradient is written (they start as NaN) and
+    sampled dQ rows and dK, dV columns of every head match the oracle."""
+    B, H, H_kv, N, d = 1, 22, 11, 4096, 64
+    q, k, v = I.make_general(B, H, H_kv, N, N, d, "bf16", seed=860, factor=0.5)
+    dout = I.make_dout(B, H, N, d, "bf16", seed=860)
+    (dq, dk, dv), sc = run_bwd(q, k, v, dout, "bf16", causal=True)
+    assert np.isfinite(dq).all() and np.isfinite(dk).all() and np.isfinite(dv).all()
+    rows = np.array([(0, h, i) for h in range(0, H, 3) for i in (5, 2100, N - 1)])
+    ref_dq = oracle.attention_bwd_dq_rows_f64(q, k, v, dout, sc, rows, causal=True)
+    e_dq = np.max(np.abs(dq[rows[:, 0], rows[:, 1], rows[:, 2]] - ref_dq)) / np.max(np.abs(ref_dq))
+    cols = np.array([(0, h, j) for h in range(H_kv) for j in (0, 3000)])
+    ref_dk, ref_dv = oracle.attention_bwd_dkv_cols_f64(q, k, v, dout, sc, cols, causal=True)
+    got = [gr[cols[:, 0], cols[:, 1], cols[:, 2]] for gr in (dk, dv)]
+    e_dk = np.max(np.abs(got[0] - ref_dk)) / np.max(np.abs(ref_dk))
+    e_dv = np.max(np.abs(got[1] - ref_dv)) / np.max(np.abs(ref_dv))
+    assert max(e_dq, e_dk, e_dv) <= tol_grad("bf16"), (e_dq, e_dk, e_dv)
