@@ -239,17 +239,24 @@ def _dtype_code(t) -> int:
 
 
 def attention(q, k, v, scale: float | None = None, out=None, lse=None, with_lse: bool = True,
-              stream=None, causal: bool = False):
-    """O = softmax(scale * Q K^T) V for CUDA tensors [B, H, N, d].
+              stream=None, causal: bool = False, num_splits: int | None = None, workspace=None):
+    """O = softmax(scale * Q K^T) V for CUDA tensors q [B, H, N_q, d] and k, v
+    [B, H_kv, N_kv, d]: H a multiple of H_kv (query head h reads key/value
+    head h // (H // H_kv)), N_q and N_kv independent (a decode step has
+    N_q = 1).  bf16, fp16 (d = 64, 128) or fp32 (d = 64, TF32 tensor cores).
 
-    Returns (out, lse); lse is fp32 [B, H, N] (natural log) or None when
-    with_lse is False.  scale defaults to 1/sqrt(d) in fp32.  Enqueued on
-    `stream` (default: PyTorch's current stream); raises FAError on a
-    non-OK status.
+    Returns (out, lse); lse is fp32 [B, H, N_q] (natural log) or None when
+    with_lse is False.  scale defaults to 1/sqrt(d) in fp32.  causal: query i
+    sees keys j <= i + N_kv - N_q.  num_splits: key-range partitions (None:
+    as many as fill one wave of the device's SMs, fa_fwd_ex_splits); their
+    workspace is allocated when not given.  Enqueued on `stream` (default:
+    PyTorch's current stream); raises FAError on a non-OK status.
     """
     import torch
-    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
-        raise ValueError(f"q, k, v must share one [B,H,N,d] shape: {q.shape} {k.shape} {v.shape}")
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape:
+        raise ValueError(f"q must be [B,H,N_q,d] and k, v one [B,H_kv,N_kv,d] shape: {q.shape} {k.shape} {v.shape}")
+    if q.shape[0] != k.shape[0] or q.shape[3] != k.shape[3] or q.shape[1] % k.shape[1] != 0:
+        raise ValueError(f"incompatible q and k/v shapes: {q.shape} {k.shape}")
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
         raise ValueError("q, k, v must be CUDA tensors")
     if not (q.dtype == k.dtype == v.dtype):
@@ -257,22 +264,31 @@ def attention(q, k, v, scale: float | None = None, out=None, lse=None, with_lse:
     for t in (q, k, v):
         if not t.is_contiguous():
             raise ValueError("q, k, v must be contiguous")
-    B, H, N, d = (int(x) for x in q.shape)
+    B, H, N_q, d = (int(x) for x in q.shape)
+    H_kv, N_kv = int(k.shape[1]), int(k.shape[2])
     if scale is None:
         scale = float(torch.tensor(1.0, dtype=torch.float32) / torch.sqrt(torch.tensor(float(d), dtype=torch.float32)))
     if not math.isfinite(scale):
         raise ValueError("scale must be finite")
+    if num_splits is None:
+        sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+        num_splits = fa_fwd_ex_splits(B, H, H_kv, N_q, N_kv, sms)
+    need = fa_fwd_ex_workspace_size(B, H, N_q, N_kv, d, num_splits)
+    if need > 0 and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     if out is None:
         out = torch.empty_like(q)
     if lse is None and with_lse:
-        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+        lse = torch.empty((B, H, N_q), dtype=torch.float32, device=q.device)
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     with torch.cuda.device(q.device):
-        st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                    lse.data_ptr() if lse is not None else None, B, H, N, d, float(scale),
-                    _dtype_code(q) | (FA_FLAG_CAUSAL if causal else 0), s.cuda_stream)
+        st = fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                       lse.data_ptr() if lse is not None else None, B, H, H_kv, N_q, N_kv, d, float(scale),
+                       _dtype_code(q) | (FA_FLAG_CAUSAL if causal else 0), num_splits,
+                       workspace.data_ptr() if need > 0 else None,
+                       workspace.numel() * workspace.element_size() if need > 0 else 0, s.cuda_stream)
     if st != FA_OK:
-        raise FAError(st, "fa_fwd")
+        raise FAError(st, "fa_fwd_ex")
     return out, lse
 
 

@@ -134,3 +134,21 @@ def test_torch_convenience_wrapper():
     torch.cuda.synchronize()
     err_o, err_l = compare(w, out.float().cpu().numpy(), lse.cpu().numpy(), q, k, v)
     assert err_o <= tol_o(w) and err_l <= TOL_LSE
+
+
+def test_torch_wrapper_general_shapes():
+    """attention() on grouped key/value heads and N_q != N_kv: a decode step
+    with its key partitions chosen for the device, and a causal fp16 case
+    with explicit partitions."""
+    import exact_tiled_attention_04_gb300 as fa
+    from .gpu_util import TOL_LSE, compare_ex, to_device, tol_o_dtype
+    q, k, v = I.make_general(2, 16, 4, 1, 5000, 128, "bf16", seed=13)
+    out, lse = fa.attention(*(to_device(x, "bf16") for x in (q, k, v)))
+    torch.cuda.synchronize()
+    err_o, err_l = compare_ex("bf16", out.float().cpu().numpy(), lse.cpu().numpy(), q, k, v)
+    assert err_o <= tol_o_dtype("bf16") and err_l <= TOL_LSE, (err_o, err_l)
+    q, k, v = I.make_general(1, 8, 2, 100, 700, 64, "f16", seed=14)
+    out, lse = fa.attention(*(to_device(x, "f16") for x in (q, k, v)), causal=True, num_splits=3)
+    torch.cuda.synchronize()
+    err_o, err_l = compare_ex("f16", out.float().cpu().numpy(), lse.cpu().numpy(), q, k, v, causal=True)
+    assert err_o <= tol_o_dtype("f16") and err_l <= TOL_LSE, (err_o, err_l)
