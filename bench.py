@@ -316,7 +316,9 @@ def config_of(w, n_gpus: int, splits: int = 1):
         cfg.update({"H_kv": w.H_kv, "N_kv": w.Nkv})
     if w.causal:
         cfg["causal"] = True
-    if splits > 1:
+    if splits == 0 and not w.backward:
+        cfg["splits"] = "automatic (fa_fwd_ex num_splits = 0: the library's plan for this GPU)"
+    elif splits > 1:
         cfg["splits"] = splits
     if w.backward:
         cfg["pass"] = "backward: dQ, dK, dV for a seeded dO (forward outputs o, lse computed once)"
@@ -356,10 +358,7 @@ def run_ours(args, w):
     if w.causal:
         dt_code |= fab.FA_FLAG_CAUSAL
     scale = float(w.scale)
-    splits = w.splits
-    if splits == 0:  # as many key partitions as fill one wave of SMs
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        splits = fab.fa_fwd_ex_splits(w.B, w.H, w.H_kv, w.N, w.Nkv, sms)
+    splits = w.splits  # 0: the library's automatic plan for this GPU
     wbytes = fab.fa_fwd_ex_workspace_size(w.B, w.H, w.N, w.Nkv, w.d, splits)
     work = torch.empty(max(wbytes, 16), dtype=torch.uint8, device=dev)  # caller-owned scratch
     launches = 0
@@ -372,7 +371,8 @@ def run_ours(args, w):
             raise fab.FAError(st, "fa_fwd_ex")
 
     if not w.backward:
-        kernels_per_step = 2 if wbytes else 1  # forward (+ merge of the partitions)
+        # forward (+ merge of the partitions; + a split last wave with the automatic plan)
+        kernels_per_step = fab.fa_fwd_ex_launches(w.B, w.H, w.H_kv, w.N, w.Nkv, w.d, dt_code, splits)
         step_fn = forward
         # end to end: fa_fwd_host on pinned host tensors (q, k, v up; o and
         # lse back, overlapped with the computation inside the call)
@@ -544,9 +544,12 @@ def run_ours(args, w):
         # the decode kernel takes 16-bit inputs with at most 32 query rows per
         # key/value head (N x H / H_kv), like the library's own dispatch
         decode = w.dtype != "f32" and w.N * (w.H // w.H_kv) <= 32
-        kernel_name = (f"{'fa_decode_kernel' if decode else 'fa_fwd_kernel'}"
-                       f"<{w.dtype},{w.d}{',causal' if w.causal else ''}>"
-                       + (" + fa_merge_kernel" if kernels_per_step == 2 else ""))
+        base = (f"{'fa_decode_kernel' if decode else 'fa_fwd_kernel'}"
+                f"<{w.dtype},{w.d}{',causal' if w.causal else ''}>")
+        if kernels_per_step == 3:
+            kernel_name = f"{base} (full waves) + {base} (last wave, split) + fa_merge_kernel"
+        else:
+            kernel_name = base + (" + fa_merge_kernel" if kernels_per_step == 2 else "")
     if intensity >= ridge:
         achieved = w.flops() / step_s / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": UNIT,

@@ -13,7 +13,7 @@ from .binding import (FA_DTYPE_BF16, FA_DTYPE_F16, FA_DTYPE_F32, FA_FLAG_CAUSAL,
                       FA_ERR_INVALID_ARG, FA_ERR_TIMEOUT, FA_ERR_UNSUPPORTED, FA_OK, FAError,
                       attention, attention_backward, fa_bwd, fa_bwd_host, fa_bwd_host_workspace_size,
                       fa_bwd_validate, fa_bwd_workspace_size, fa_device_status, fa_fwd, fa_fwd_ex,
-                      fa_fwd_ex_splits, fa_fwd_ex_static, fa_fwd_ex_static_capacity, fa_fwd_ex_validate,
+                      fa_fwd_ex_launches, fa_fwd_ex_splits, fa_fwd_ex_static, fa_fwd_ex_static_capacity, fa_fwd_ex_validate,
                       fa_fwd_ex_workspace_size, fa_fwd_host, fa_fwd_host_workspace_size, fa_fwd_validate,
                       fa_last_error_message, fa_selftest_barrier_timeout, fa_status_string,
                       fa_version)

@@ -88,6 +88,8 @@ def load(path: str | None = None):
         lib.fa_fwd_ex_workspace_size.argtypes = [i64, i64, i64, i64, i64, c_int]
         lib.fa_fwd_ex_splits.restype = c_int
         lib.fa_fwd_ex_splits.argtypes = [i64, i64, i64, i64, i64, c_int]
+        lib.fa_fwd_ex_launches.restype = c_int
+        lib.fa_fwd_ex_launches.argtypes = [i64, i64, i64, i64, i64, i64, c_int, c_int]
         lib.fa_fwd_ex_static.restype = c_int
         lib.fa_fwd_ex_static.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, c_int,
                                          c_int, vp]
@@ -151,6 +153,11 @@ def fa_fwd_ex_workspace_size(B: int, H: int, N_q: int, N_kv: int, d: int, num_sp
 
 def fa_fwd_ex_splits(B: int, H: int, H_kv: int, N_q: int, N_kv: int, num_sms: int) -> int:
     return int(load().fa_fwd_ex_splits(B, H, H_kv, N_q, N_kv, num_sms))
+
+
+def fa_fwd_ex_launches(B: int, H: int, H_kv: int, N_q: int, N_kv: int, d: int, dtype: int,
+                       num_splits: int) -> int:
+    return load().fa_fwd_ex_launches(B, H, H_kv, N_q, N_kv, d, dtype, num_splits)
 
 
 def fa_fwd_ex_static(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, H_kv: int,
@@ -248,8 +255,8 @@ def attention(q, k, v, scale: float | None = None, out=None, lse=None, with_lse:
     Returns (out, lse); lse is fp32 [B, H, N_q] (natural log) or None when
     with_lse is False.  scale defaults to 1/sqrt(d) in fp32.  causal: query i
     sees keys j <= i + N_kv - N_q.  num_splits: key-range partitions (None:
-    as many as fill one wave of the device's SMs, fa_fwd_ex_splits); their
-    workspace is allocated when not given.  Enqueued on `stream` (default:
+    the library's automatic plan for the device, num_splits = 0 of
+    fa_fwd_ex); their workspace is allocated when not given.  Enqueued on `stream` (default:
     PyTorch's current stream); raises FAError on a non-OK status.
     """
     import torch
@@ -271,9 +278,9 @@ def attention(q, k, v, scale: float | None = None, out=None, lse=None, with_lse:
     if not math.isfinite(scale):
         raise ValueError("scale must be finite")
     if num_splits is None:
-        sms = torch.cuda.get_device_properties(q.device).multi_processor_count
-        num_splits = fa_fwd_ex_splits(B, H, H_kv, N_q, N_kv, sms)
-    need = fa_fwd_ex_workspace_size(B, H, N_q, N_kv, d, num_splits)
+        num_splits = 0  # the library's automatic plan for this device
+    with torch.cuda.device(q.device):
+        need = fa_fwd_ex_workspace_size(B, H, N_q, N_kv, d, num_splits)
     if need > 0 and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     if out is None:

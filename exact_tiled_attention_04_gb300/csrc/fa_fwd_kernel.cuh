@@ -295,12 +295,11 @@ __device__ __forceinline__ float sum8(const uint64_t (&a)[4]) {
 template <int D>
 __device__ __noinline__ void store_partial(const FwdParams& p, uint32_t tO, long long qrow, float m_ref,
                                            float l, float lq) {
-    // qrow: the query row's index in a partition's slab (B*H*Nq rows), or -1
-    // for a tile row that is not a query row
+    // qrow: the query row's output row (of B*H*Nq), or -1 for a tile row
+    // that is not a query row; a partition's slab holds rows part_row0 ..
+    // part_row0 + part_rows - 1
     const unsigned int split = blockIdx.x % static_cast<unsigned>(p.splits);
-    const size_t slab = static_cast<size_t>(gridDim.x / p.splits / p.n_q_blocks) * p.Nq *
-                        (p.pack ? static_cast<size_t>(p.group) : 1u);
-    const size_t r = split * slab + static_cast<size_t>(qrow);
+    const size_t r = split * static_cast<size_t>(p.part_rows) + static_cast<size_t>(qrow - p.part_row0);
 #pragma unroll
     for (int q = 0; q < D / 32; ++q) {
         uint32_t o[32];
@@ -474,7 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // grouped heads packed into query tile 0 (p.pack; always set when kOneTile)
     const bool pack = kOneTile || p.pack != 0;
     const unsigned int split = blockIdx.x % static_cast<unsigned>(p.splits);
-    const unsigned int cta = blockIdx.x / static_cast<unsigned>(p.splits);
+    // (a tail launch starts at query block p.item_offset; unmasked launches only)
+    const unsigned int cta = blockIdx.x / static_cast<unsigned>(p.splits) + static_cast<unsigned>(p.item_offset);
     int qb, bh;
     if (kCausal) {
         // later query blocks see more keys: heaviest first, by groups of heads
@@ -940,9 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 store_partial<D>(p, tO, out_row, m_ref, l, lq);
             } else if (out_row >= 0) {
                 // an empty partition: weight 0 in the merge (its O slot is not read)
-                const size_t slab = static_cast<size_t>(gridDim.x / p.splits / p.n_q_blocks) * p.Nq *
-                                    (pack ? static_cast<size_t>(p.group) : 1u);
-                const size_t r = split * slab + static_cast<size_t>(out_row);
+                const size_t r = split * static_cast<size_t>(p.part_rows) + static_cast<size_t>(out_row - p.part_row0);
                 *reinterpret_cast<float4*>(p.ml_part + r * 4) = make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
             }
         }

@@ -42,6 +42,10 @@ struct FwdParams {
     float* o_part;           // fp32 [splits, B*H, Nq, d]
     float* ml_part;          // fp32 [splits, B*H, Nq, 4]: m (base 2, scaled), l, lq, unused
     void* out;               // decode kernel, splits == 1: O [B*H, Nq, d] (input dtype)
+    int item_offset;         // first query block (work item) of this launch: 0, or the
+                             // first block of a tail launch (see launch_ex)
+    long long part_row0;     // splits > 1: output row of the first row of a partition's slab
+    long long part_rows;     // splits > 1: rows of one partition's slab
 };
 
 // Merge of split partial results: O = sum_s w_s O_s / sum_s w_s lq_s,

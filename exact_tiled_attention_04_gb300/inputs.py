@@ -140,7 +140,7 @@ class Workload:
     H_kv: int = 0          # key/value heads (0: H, plain multi-head attention)
     Nkv: int = 0           # key/value rows per head (0: N; N is the query rows)
     causal: bool = False   # query i sees keys j <= i + Nkv - N only
-    splits: int = 1        # key-range partitions (0: as many as fill one wave)
+    splits: int = 0        # key-range partitions (0: the library's plan for the device)
     backward: bool = False  # the step is the backward pass (dQ, dK, dV) for a fixed dO
     scale: np.float32 = field(init=False)
 
@@ -191,10 +191,10 @@ class Workload:
 
 WORKLOADS = {
     "single_head_n512": Workload(
-        "single_head_n512", 1, 1, 512, 64, "f32", seed=1, splits=0,
+        "single_head_n512", 1, 1, 512, 64, "f32", seed=1,
         note="single head, fp32 inputs and output"),
     "tail_n1000": Workload(
-        "tail_n1000", 2, 4, 1000, 64, "bf16", seed=2, splits=0,
+        "tail_n1000", 2, 4, 1000, 64, "bf16", seed=2,
         identical_k_heads=((0, 1),), q_scaled_heads=((1, 2, 30.0),),
         note="N not a multiple of the tile; one head with identical keys, one with Q x30"),
     "b4h16_n2048": Workload("b4h16_n2048", 4, 16, 2048, 64, "bf16", seed=3),
@@ -214,7 +214,7 @@ WORKLOADS["b1h32_n8192_d128"] = Workload(
 # 16k-key cache (FlashDecoding: the keys split across the GPU), the headline
 # shape with 4:1 grouped key/value heads, with the causal mask, and in fp16.
 WORKLOADS["decode_b8h32kv8_n16384_d128"] = Workload(
-    "decode_b8h32kv8_n16384_d128", 8, 32, 1, 128, "bf16", seed=7, H_kv=8, Nkv=16384, splits=0,
+    "decode_b8h32kv8_n16384_d128", 8, 32, 1, 128, "bf16", seed=7, H_kv=8, Nkv=16384,
     note="one query per head against a 16k-key cache, grouped heads, split-KV")
 WORKLOADS["gqa_b2h32kv8_n8192_d128"] = Workload(
     "gqa_b2h32kv8_n8192_d128", 2, 32, 8192, 128, "bf16", seed=8, factor=0.5, H_kv=8,

@@ -110,6 +110,14 @@ int fa_fwd_validate(const void* q, const void* k, const void* v, void* o,
  *             small; their partial results go to `workspace` and a second
  *             kernel merges them with the online-softmax rescaling.  The
  *             count is capped at 32 and at one partition per 128 keys.
+ *             0 chooses automatically for the current device (one CTA per
+ *             SM): a launch with fewer query blocks than SMs gets the
+ *             fa_fwd_ex_splits count; a launch of several waves whose last
+ *             wave is at most half full (16-bit inputs, unmasked, query
+ *             heads not packed, N_kv >= 4096) runs the full waves unsplit and the last
+ *             wave's query blocks in a second launch split along the keys
+ *             (up to 4 partitions), merged over their rows; otherwise one
+ *             partition.
  *   workspace, workspace_bytes: device scratch owned by the caller, 16-byte
  *             aligned, at least fa_fwd_ex_workspace_size(...) bytes; may be
  *             NULL when that size is 0.  Contents on entry do not matter.
@@ -122,7 +130,8 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
               int64_t d, float scale, int dtype, int num_splits,
               void* workspace, size_t workspace_bytes, void* stream);
 
-/* Host-side argument checks of fa_fwd_ex alone (no CUDA call). */
+/* Host-side argument checks of fa_fwd_ex alone (no CUDA call, except the
+ * SM-count query of the current device when num_splits = 0). */
 int fa_fwd_ex_validate(const void* q, const void* k, const void* v, void* o,
                        const float* lse, int64_t B, int64_t H, int64_t H_kv,
                        int64_t N_q, int64_t N_kv, int64_t d, float scale,
@@ -132,7 +141,10 @@ int fa_fwd_ex_validate(const void* q, const void* k, const void* v, void* o,
 /*
  * Workspace bytes fa_fwd_ex needs for `num_splits` (after the same capping):
  * splits * B * H * N_q * (d + 4) * 4, or 0 when one partition remains.
- * Pure host computation; 0 for invalid sizes.
+ * Pure host computation; 0 for invalid sizes.  num_splits = 0 (automatic):
+ * a bound for every plan on the current device, min(SMs * 256,
+ * 32 * B * H * N_q) * (d + 4) * 4 (SMs taken as 1024 when no device answers;
+ * the SM count is the one CUDA query here).
  */
 size_t fa_fwd_ex_workspace_size(int64_t B, int64_t H, int64_t N_q, int64_t N_kv,
                                 int64_t d, int num_splits);
@@ -147,6 +159,16 @@ size_t fa_fwd_ex_workspace_size(int64_t B, int64_t H, int64_t N_q, int64_t N_kv,
  */
 int fa_fwd_ex_splits(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv,
                      int num_sms);
+
+/*
+ * Kernel launches fa_fwd_ex enqueues for these arguments: 1 (one key
+ * partition), 2 (partitions and their merge), or 3 (num_splits = 0 with a
+ * split tail: the full waves, the tail's partitions, their merge); 0 for
+ * invalid sizes.  For num_splits = 0 the plan is the current device's (the
+ * SM-count query is the one CUDA call here).
+ */
+int fa_fwd_ex_launches(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv,
+                       int64_t d, int dtype, int num_splits);
 
 /*
  * fa_fwd_ex_static — fa_fwd_ex for callers that cannot allocate device

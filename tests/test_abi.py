@@ -112,7 +112,8 @@ def test_ex_validation(lib):
     assert validate_ex(H_kv=3) == fab.FA_ERR_INVALID_ARG          # 8 query heads, 3 kv heads
     assert validate_ex(H_kv=0) == fab.FA_ERR_INVALID_ARG
     assert validate_ex(Nq=0) == fab.FA_ERR_INVALID_ARG
-    assert validate_ex(splits=0) == fab.FA_ERR_INVALID_ARG
+    assert validate_ex(splits=-1) == fab.FA_ERR_INVALID_ARG
+    assert validate_ex(splits=0) == fab.FA_OK  # automatic (no device here: one partition)
     need = fab.fa_fwd_ex_workspace_size(2, 8, 1, 4096, 128, 8)
     assert need == 8 * 2 * 8 * 1 * (128 + 4) * 4
     assert validate_ex(splits=8) == fab.FA_ERR_INVALID_ARG          # workspace missing

@@ -99,15 +99,29 @@ def test_workspace_too_small_is_rejected():
     assert st == fab.FA_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("name", ["single_head_n512", "tail_n1000", "decode_b8h32kv8_n16384_d128"])
+BENCH_FORWARD = [n for n, w in I.WORKLOADS.items() if not w.backward]
+
+
+@pytest.mark.parametrize("name", BENCH_FORWARD)
 def test_workloads_in_bench_launch_configuration(name):
-    """The small workloads and the decode workload as the benchmark launches
-    them: fa_fwd_ex with the key partitions that fill one wave of SMs."""
+    """Every forward workload as the benchmark launches it: fa_fwd_ex with
+    the workload's num_splits (0: the library's plan for this device, which
+    on a 152-SM GPU splits the last wave of the headline shapes).  Every
+    output row must be written; the small workloads are compared on every
+    row, the large ones on seeded rows, the edge rows and rows of the last
+    three heads (the ones a split last wave covers)."""
+    from .gpu_util import edge_rows
     w = I.WORKLOADS[name]
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    splits = fab.fa_fwd_ex_splits(w.B, w.H, w.H_kv, w.N, w.Nkv, sms) if w.splits == 0 else w.splits
     q, k, v = I.make(w)
-    check(w.dtype, q, k, v, splits)
+    o, lse = run_fa_ex(q, k, v, w.dtype, w.splits, causal=w.causal)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    rows = None
+    if w.oracle_rows is not None:
+        tail = [(w.B - 1, h, i) for h in range(max(0, w.H - 3), w.H)
+                for i in (0, 1, w.N // 2, w.N - 2, w.N - 1)]
+        rows = np.concatenate([edge_rows(w, w.oracle_rows), np.array(tail, dtype=np.int64)])
+    err_o, err_l = compare_ex(w.dtype, o, lse, q, k, v, rows=rows, causal=w.causal)
+    assert err_o <= tol_o_dtype(w.dtype) and err_l <= TOL_LSE, (name, err_o, err_l)
 
 
 @pytest.mark.parametrize("name", ["gqa_b2h32kv8_n8192_d128", "causal_b2h32_n8192_d128",
@@ -143,3 +157,20 @@ def test_packed_causal_and_fp32():
     check("f32", q, k, v, 2)
     q, k, v = I.make_general(2, 16, 4, 1, 3000, 64, "f16", seed=522)
     check("f16", q, k, v, 4)
+
+
+@pytest.mark.parametrize("B,H,H_kv,N,d,dtype", [
+    (1, 10, 10, 4096, 64, "bf16"),    # 160 blocks: 152 unsplit, the last 8 of one head split
+    (1, 10, 10, 4500, 128, "bf16"),   # 180 blocks: the split tail crosses a head, ragged last blocks
+    (1, 20, 5, 4096, 64, "f16"),      # grouped heads, 320 blocks, a tail of 16
+    (1, 6, 6, 3000, 64, "bf16"),      # 72 blocks (one partial wave): partitions of every block
+])
+def test_automatic_partitions(B, H, H_kv, N, d, dtype):
+    """num_splits = 0: the library plans the partitions for the device (on a
+    152-SM GB300 these shapes run their last wave as a split second launch
+    merged over its rows); every output row matches the oracle."""
+    q, k, v = I.make_general(B, H, H_kv, N, N, d, dtype, seed=980 + H + d)
+    o, lse = run_fa_ex(q, k, v, dtype, 0)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    err_o, err_l = compare_ex(dtype, o, lse, q, k, v)
+    assert err_o <= tol_o_dtype(dtype) and err_l <= TOL_LSE, (err_o, err_l)
