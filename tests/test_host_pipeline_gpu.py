@@ -1,8 +1,10 @@
 """fa_fwd_host: the forward pass on host tensors with overlapped copies.
 
-Each chunk is an ordinary fa_fwd_ex launch on device copies of contiguous
-head ranges, so the outputs must equal fa_fwd_ex on the whole problem bit for
-bit; they are also compared with the oracle on sampled rows."""
+Each chunk is an ordinary fa_fwd_ex launch (with the library's automatic key
+partitions) on device copies of contiguous head ranges, so the outputs equal
+fa_fwd_ex on the whole problem up to the summation order of the partitions
+(bit for bit where no chunk is split); they are also compared with the oracle
+on sampled rows."""
 import numpy as np
 import pytest
 
@@ -49,12 +51,20 @@ def run_host(q, k, v, dtype, causal=False, with_lse=True):
     (2, 17, 17, 257, 129, 128, "bf16", True),    # ragged last chunk
     (4, 16, 4, 1, 700, 128, "bf16", False),      # decode: packed grouped heads
     (2, 4, 4, 160, 160, 64, "f32", False),       # TF32 path
+    (2, 40, 40, 2048, 2048, 64, "bf16", False),  # 80 units: ramp chunks of 4 and 8 units, split
+    (2, 40, 40, 2048, 2048, 128, "f16", True),   # ramp chunks of 2 and 4 units, causal
 ])
 def test_matches_device_call(B, H, H_kv, Nq, Nkv, d, dtype, causal):
     q, k, v = I.make_general(B, H, H_kv, Nq, Nkv, d, dtype, seed=700 + H + Nq)
     o_h, l_h = run_host(q, k, v, dtype, causal)
     o_d, l_d = run_fa_ex(q, k, v, dtype, 1, causal=causal)
-    assert np.array_equal(o_h, o_d) and np.array_equal(l_h, l_d)
+    # partitions change only the order of the fp32 sums: within an output
+    # rounding step of the unsplit result
+    # (rows that see no key: O = 0 and lse = -inf on both sides)
+    assert not np.isnan(o_h).any() and not np.isnan(l_h).any()
+    assert np.array_equal(np.isneginf(l_h), np.isneginf(l_d))
+    seen = np.isfinite(l_d)
+    assert np.max(np.abs(o_h - o_d)) <= 2 ** -7 and np.max(np.abs(l_h[seen] - l_d[seen])) <= 1e-4
     rng = np.random.default_rng(5)
     rows = np.stack([rng.integers(0, B, 16), rng.integers(0, H, 16), rng.integers(0, Nq, 16)], axis=1)
     err_o, err_l = compare_ex(dtype, o_h, l_h, q, k, v, rows=rows, causal=causal)
@@ -72,6 +82,7 @@ def test_without_lse_and_repeated():
     (1, 2, 2, 300, 333, 64, "bf16", False),      # one chunk
     (2, 8, 2, 200, 260, 128, "bf16", True),      # grouped heads
     (4, 16, 16, 256, 1024, 64, "f16", False),    # several chunks
+    (2, 36, 36, 1024, 1024, 64, "bf16", False),  # 72 units: ramp chunks
 ])
 def test_backward_matches_device_call(B, H, H_kv, Nq, Nkv, d, dtype, causal):
     """fa_bwd_host equals fa_bwd on device copies up to the summation order
