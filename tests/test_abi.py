@@ -139,6 +139,20 @@ def test_split_planning(lib):
     assert fab.fa_fwd_ex_splits(1, 8, 2, 64, 4096, 152) == 16       # 64 x 4 rows > 128: 8 CTAs; 19 wanted, 2 of 32 tiles each
 
 
+def test_launch_counts(lib):
+    bf16 = fab.FA_DTYPE_BF16
+    # explicit partitions: one launch, or the split launch and its merge
+    assert fab.fa_fwd_ex_launches(1, 1, 1, 100, 1000, 64, bf16, 1) == 1
+    assert fab.fa_fwd_ex_launches(1, 1, 1, 100, 1000, 64, bf16, 4) == 2
+    assert fab.fa_fwd_ex_launches(1, 1, 1, 100, 100, 64, bf16, 4) == 1   # one key tile: no split
+    # automatic plan without a device to ask: one partition
+    assert fab.fa_fwd_ex_launches(2, 32, 32, 8192, 8192, 128, bf16, 0) == 1
+    # invalid sizes
+    assert fab.fa_fwd_ex_launches(1, 3, 2, 100, 100, 64, bf16, 1) == 0
+    assert fab.fa_fwd_ex_launches(1, 1, 1, 100, 100, 64, bf16, -1) == 0
+    assert fab.fa_fwd_ex_launches(0, 1, 1, 100, 100, 64, bf16, 1) == 0
+
+
 def test_dtype_flags(lib):
     assert validate(dtype=fab.FA_DTYPE_F16) == fab.FA_OK
     assert validate(dtype=fab.FA_DTYPE_F16, d=128) == fab.FA_OK

@@ -159,6 +159,23 @@ def test_packed_causal_and_fp32():
     check("f16", q, k, v, 4)
 
 
+def test_automatic_plan_launch_counts():
+    """The plan on this device: the headline shape on a 152-SM GPU runs its
+    13 full waves unsplit and its last 72 blocks split (3 launches); causal
+    and fp32 launches never take the split last wave; an underfilled launch
+    splits every block (2 launches)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    bf16, f32, causal = fab.FA_DTYPE_BF16, fab.FA_DTYPE_F32, fab.FA_FLAG_CAUSAL
+    blocks = 2 * 32 * 32
+    last = blocks % sms
+    expect = 3 if 0 < last and 2 * last <= sms else 1
+    assert fab.fa_fwd_ex_launches(2, 32, 32, 8192, 8192, 128, bf16, 0) == expect
+    assert fab.fa_fwd_ex_launches(2, 32, 32, 8192, 8192, 128, bf16 | causal, 0) == 1
+    assert fab.fa_fwd_ex_launches(4, 16, 16, 2048, 2048, 64, bf16, 0) == 1   # 16 key tiles: not split
+    assert fab.fa_fwd_ex_launches(1, 1, 1, 512, 512, 64, f32, 0) == 2
+    assert fab.fa_fwd_ex_launches(8, 32, 8, 1, 16384, 128, bf16, 0) == 2     # decode: 64 CTAs, 2 partitions
+
+
 @pytest.mark.parametrize("B,H,H_kv,N,d,dtype", [
     (1, 10, 10, 4096, 64, "bf16"),    # 160 blocks: 152 unsplit, the last 8 of one head split
     (1, 10, 10, 4500, 128, "bf16"),   # 180 blocks: the split tail crosses a head, ragged last blocks
