@@ -112,18 +112,19 @@ int fa_fwd_validate(const void* q, const void* k, const void* v, void* o,
  *             count is capped at 32 and at one partition per 128 keys.
  *             0 chooses automatically for the current device (one CTA per
  *             SM): a launch with fewer query blocks than SMs gets the
- *             fa_fwd_ex_splits count; a launch of several waves whose last
- *             wave is at most half full (16-bit inputs, unmasked, query
- *             heads not packed, N_kv >= 4096) runs the full waves unsplit and the last
- *             wave's query blocks in a second launch split along the keys
- *             (up to 4 partitions), merged over their rows; otherwise one
- *             partition.
+ *             fa_fwd_ex_splits count; a launch of several waves whose
+ *             last wave is at most half full (16-bit inputs, unmasked,
+ *             query heads not packed, N_kv >= 4096) runs the full waves
+ *             unsplit and the last wave's query blocks in a second launch
+ *             split along the keys (up to 4 partitions), merged over their
+ *             rows; otherwise one partition.
  *   workspace, workspace_bytes: device scratch owned by the caller, 16-byte
  *             aligned, at least fa_fwd_ex_workspace_size(...) bytes; may be
  *             NULL when that size is 0.  Contents on entry do not matter.
  *
  * Same ownership, validation and error behaviour as fa_fwd; the workspace
- * must not overlap any tensor.  Both kernels are enqueued on `stream`.
+ * must not overlap any tensor.  Every kernel of the call (one to three, see
+ * fa_fwd_ex_launches) is enqueued on `stream`.
  */
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
               int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv,
