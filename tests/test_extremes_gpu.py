@@ -1,7 +1,8 @@
 """Extreme sizes against the oracle on sampled outputs: very long sequences
-(forward N = 131072, backward N = 16384), very many short heads (4096 heads
-of 64 rows: one ragged tile each), and a decode step against a 262144-key
-cache with one key/value head for eight query heads (MQA)."""
+(forward N = 131072, backward N = 16384), query and output tensors larger
+than 2 GiB, very many short heads (4096 heads of 64 rows: one ragged tile
+each), and a decode step against a 262144-key cache with one key/value head
+for eight query heads (MQA)."""
 import numpy as np
 import pytest
 
@@ -38,6 +39,21 @@ def test_forward_long_sequence(N, d):
         rows = sample_rows(1, 1, N, 12, 801)
         err_o, err_l = compare_ex("bf16", o, lse, q, k, v, rows=rows, causal=causal)
         assert err_o <= tol_o_dtype("bf16") and err_l <= TOL_LSE, (causal, err_o, err_l)
+
+
+def test_forward_query_tensor_over_2_gib():
+    """q and o of 264 x 32768 x 128 bf16 elements (2.2 GB each, byte offsets
+    past 2^31) against one key/value head, in the automatic plan (which
+    splits the last 48 of 33792 query blocks): rows at the far end of the
+    tensors match the oracle."""
+    B, H, H_kv, N, d = 1, 264, 1, 32768, 128
+    q, k, v = I.make_general(B, H, H_kv, N, N, d, "bf16", seed=850, factor=0.5)
+    o, lse = run_fa_ex(q, k, v, "bf16", 0)
+    rows = sample_rows(B, H, N, 12, 851)
+    rows = np.concatenate([rows, np.array([(0, H - 1, N - 2), (0, H - 2, N - 1), (0, H - 9, 0)])])
+    err_o, err_l = compare_ex("bf16", o, lse, q, k, v, rows=rows)
+    assert err_o <= tol_o_dtype("bf16") and err_l <= TOL_LSE, (err_o, err_l)
+    assert np.isfinite(o[0, -48:]).all() and np.isfinite(lse[0, -48:]).all()
 
 
 def test_forward_many_short_heads():
