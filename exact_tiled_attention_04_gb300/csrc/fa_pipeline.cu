@@ -30,7 +30,14 @@ using namespace fa::host;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kSlots = 3;             // chunks resident at once (in, compute, out)
+// Chunks resident at once (being copied in, computed, copied out).  The
+// backward pass's chunks take longer from their first copy in to their last
+// copy out than their copies in alone, so a fourth slot keeps its copies in
+// running (headline backward end to end 5.60 -> 5.19 ms); the forward pass
+// measured no gain from it.
+constexpr int kFwdSlots = 3;
+constexpr int kBwdSlots = 4;
+constexpr int kMaxSlots = 4;
 // Chunks of about 128 CTAs, at most 16: the first upload and the last
 // download are the only copies nothing overlaps, and smaller chunks shorten
 // them (measured against 256 CTAs / 8 chunks: headline forward 2.450 ->
@@ -46,7 +53,7 @@ constexpr int kComputeStreams = 2;   // chunk kernels alternate between them
 struct DeviceStreams {
     cudaStream_t in = nullptr, out = nullptr, comp[kComputeStreams] = {};
     cudaEvent_t start = nullptr;
-    cudaEvent_t loaded[kSlots] = {}, computed[kSlots] = {}, freed[kSlots] = {};
+    cudaEvent_t loaded[kMaxSlots] = {}, computed[kMaxSlots] = {}, freed[kMaxSlots] = {};
     bool ready = false;
 };
 DeviceStreams g_streams[kMaxDevices];
@@ -66,7 +73,7 @@ int device_streams(DeviceStreams** out, int* dev_out) {
         for (int i = 0; i < kComputeStreams && e == cudaSuccess; ++i)
             e = cudaStreamCreateWithFlags(&ds.comp[i], cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ds.start, cudaEventDisableTiming);
-        for (int i = 0; i < kSlots && e == cudaSuccess; ++i) {
+        for (int i = 0; i < kMaxSlots && e == cudaSuccess; ++i) {
             e = cudaEventCreateWithFlags(&ds.loaded[i], cudaEventDisableTiming);
             if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ds.computed[i], cudaEventDisableTiming);
             if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ds.freed[i], cudaEventDisableTiming);
@@ -272,7 +279,7 @@ size_t fa_fwd_host_workspace_size(int64_t B, int64_t H, int64_t H_kv, int64_t N_
     if (B > INT64_MAX / H || B * H > INT64_MAX / N_q || B * H * N_q > INT64_MAX / (d * 4)) return 0;
     if (B * H_kv > INT64_MAX / N_kv || B * H_kv * N_kv > INT64_MAX / (d * 4)) return 0;
     const Plan pl = make_plan(B, H, H_kv, N_q, N_kv, d, dtype);
-    return static_cast<size_t>(pl.chunks < kSlots ? pl.chunks : kSlots) * pl.slot_bytes;
+    return static_cast<size_t>(pl.chunks < kFwdSlots ? pl.chunks : kFwdSlots) * pl.slot_bytes;
 }
 
 int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
@@ -285,7 +292,7 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
     if (workspace == nullptr) return FA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGNMENT;
     const Plan pl = make_plan(B, H, H_kv, N_q, N_kv, d, dtype);
-    const int slots = static_cast<int>(pl.chunks < kSlots ? pl.chunks : kSlots);
+    const int slots = static_cast<int>(pl.chunks < kFwdSlots ? pl.chunks : kFwdSlots);
     const size_t ws_need = static_cast<size_t>(slots) * pl.slot_bytes;
     if (workspace_bytes < ws_need) return FA_ERR_INVALID_ARG;
     {
@@ -339,7 +346,7 @@ size_t fa_bwd_host_workspace_size(int64_t B, int64_t H, int64_t H_kv, int64_t N_
     if (B > INT64_MAX / H || B * H > INT64_MAX / (N_q + 128) || B * H * (N_q + 128) > INT64_MAX / (d * 4)) return 0;
     if (B * H_kv > INT64_MAX / N_kv || B * H_kv * N_kv > INT64_MAX / (d * 4)) return 0;
     const BwdPlan pl = make_bwd_plan(B, H, H_kv, N_q, N_kv, d);
-    return static_cast<size_t>(pl.chunks < kSlots ? pl.chunks : kSlots) * pl.slot_bytes;
+    return static_cast<size_t>(pl.chunks < kBwdSlots ? pl.chunks : kBwdSlots) * pl.slot_bytes;
 }
 
 int fa_bwd_host(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -352,7 +359,7 @@ int fa_bwd_host(const void* q, const void* k, const void* v, const void* o, cons
     if (st != FA_OK) return st;
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_ALIGNMENT;
     const BwdPlan pl = make_bwd_plan(B, H, H_kv, N_q, N_kv, d);
-    const int slots = static_cast<int>(pl.chunks < kSlots ? pl.chunks : kSlots);
+    const int slots = static_cast<int>(pl.chunks < kBwdSlots ? pl.chunks : kBwdSlots);
     const size_t ws_need = static_cast<size_t>(slots) * pl.slot_bytes;
     if (workspace_bytes < ws_need) return FA_ERR_INVALID_ARG;
     {

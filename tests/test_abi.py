@@ -213,13 +213,13 @@ def test_host_pipeline_validation(lib):
 
 def test_host_pipeline_workspace_is_checked_with_its_own_size(lib):
     """The host pipelines check their device workspace with the size they
-    need, not the (larger) workspace of the device entry point on the whole
-    problem: a tensor placed right after the pipeline workspace is accepted,
-    one that reaches into it is rejected."""
+    need, not the workspace of the device entry point on the whole problem
+    (a different size): a tensor placed right after the pipeline workspace
+    is accepted, one that reaches into its last bytes is rejected."""
     B, H, N, d = 2, 32, 8192, 128
     code = fab.FA_DTYPE_BF16
     need = fab.fa_bwd_host_workspace_size(B, H, H, N, N, d)
-    assert 0 < need < fab.fa_bwd_workspace_size(B, H, N, d)
+    assert 0 < need and need != fab.fa_bwd_workspace_size(B, H, N, d)
     qb = B * H * N * d * 2
     lb = B * H * N * 4
     ws = 1 << 40
