@@ -1,8 +1,8 @@
 """Extreme sizes against the oracle on sampled outputs: very long sequences
-(forward N = 131072, backward N = 16384), query and output tensors larger
-than 2 GiB, very many short heads (4096 heads of 64 rows: one ragged tile
-each), and a decode step against a 262144-key cache with one key/value head
-for eight query heads (MQA)."""
+(forward N = 131072, backward N = 16384), tensors past 2 GiB (the forward's
+query and output, the backward's dQ accumulator), very many short heads
+(4096 heads of 64 rows: one ragged tile each), and a decode step against a
+262144-key cache with one key/value head for eight query heads (MQA)."""
 import numpy as np
 import pytest
 
@@ -88,6 +88,27 @@ def test_backward_long_sequence():
     e_dk = np.max(np.abs(got[0] - ref_dk)) / np.max(np.abs(ref_dk))
     e_dv = np.max(np.abs(got[1] - ref_dv)) / np.max(np.abs(ref_dv))
     assert max(e_dq, e_dk, e_dv) <= tol_grad("bf16"), (e_dq, e_dk, e_dv)
+
+
+def test_backward_accumulator_over_2_gib():
+    """136 heads x 32768 rows x d = 128: q, dO and the gradients are 1.1 GB
+    each and dQ's fp32 accumulator 2.3 GB (byte offsets past 2^31); dq rows
+    at the far end and dK, dV of two keys of the last head match the oracle."""
+    B, H, N, d = 1, 136, 32768, 128
+    q, k, v = I.make_general(B, H, H, N, N, d, "bf16", seed=860, factor=0.5)
+    dout = I.make_dout(B, H, N, d, "bf16", seed=860)
+    (dq, dk, dv), sc = run_bwd(q, k, v, dout, "bf16")
+    rows = np.concatenate([sample_rows(B, H, N, 6, 861),
+                           np.array([(0, H - 1, N - 1), (0, H - 1, N - 2), (0, H - 2, 0)])])
+    ref_dq = oracle.attention_bwd_dq_rows_f64(q, k, v, dout, sc, rows)
+    e_dq = np.max(np.abs(dq[rows[:, 0], rows[:, 1], rows[:, 2]] - ref_dq)) / np.max(np.abs(ref_dq))
+    cols = np.array([(0, H - 1, N - 1), (0, H - 1, 5)])
+    ref_dk, ref_dv = oracle.attention_bwd_dkv_cols_f64(q, k, v, dout, sc, cols)
+    got = [g[cols[:, 0], cols[:, 1], cols[:, 2]] for g in (dk, dv)]
+    e_dk = np.max(np.abs(got[0] - ref_dk)) / np.max(np.abs(ref_dk))
+    e_dv = np.max(np.abs(got[1] - ref_dv)) / np.max(np.abs(ref_dv))
+    assert max(e_dq, e_dk, e_dv) <= tol_grad("bf16"), (e_dq, e_dk, e_dv)
+    assert np.isfinite(dq[0, -2:]).all() and np.isfinite(dk[0, -2:]).all() and np.isfinite(dv[0, -2:]).all()
 
 
 def test_backward_many_short_heads():
