@@ -24,18 +24,19 @@ def lib():
     return ensure_library()
 
 
-def run_host(q, k, v, dtype, causal=False, with_lse=True):
+def run_host(q, k, v, dtype, causal=False, with_lse=True, pinned=True, stream=None):
     B, H, Nq, d = q.shape
     H_kv, Nkv = k.shape[1], k.shape[2]
-    hq, hk, hv = (to_device(x, dtype).cpu().pin_memory() for x in (q, k, v))
-    ho = torch.full_like(hq, float("nan")).pin_memory()
-    hl = torch.full((B, H, Nq), float("nan"), dtype=torch.float32).pin_memory() if with_lse else None
+    pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+    hq, hk, hv = (pin(to_device(x, dtype).cpu()) for x in (q, k, v))
+    ho = pin(torch.full_like(hq, float("nan")))
+    hl = pin(torch.full((B, H, Nq), float("nan"), dtype=torch.float32)) if with_lse else None
     code = DTYPE_CODES[dtype] | (fab.FA_FLAG_CAUSAL if causal else 0)
     need = fab.fa_fwd_host_workspace_size(B, H, H_kv, Nq, Nkv, d, code)
     ws = torch.empty(need + 256, dtype=torch.uint8, device="cuda")
     base = (ws.data_ptr() + 255) // 256 * 256
     sc = float(np.float32(1.0 / np.sqrt(d)))
-    s = torch.cuda.current_stream()
+    s = stream if stream is not None else torch.cuda.current_stream()
     st = fab.fa_fwd_host(hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), ho.data_ptr(),
                          hl.data_ptr() if hl is not None else None, B, H, H_kv, Nq, Nkv, d, sc, code, base,
                          need, s.cuda_stream)
@@ -69,6 +70,44 @@ def test_matches_device_call(B, H, H_kv, Nq, Nkv, d, dtype, causal):
     rows = np.stack([rng.integers(0, B, 16), rng.integers(0, H, 16), rng.integers(0, Nq, 16)], axis=1)
     err_o, err_l = compare_ex(dtype, o_h, l_h, q, k, v, rows=rows, causal=causal)
     assert err_o <= tol_o_dtype(dtype) and err_l <= TOL_LSE
+
+
+def test_pageable_host_memory():
+    """Host tensors that are not pinned: the copies run through the
+    driver's staging buffers, and the result is the same."""
+    q, k, v = I.make_general(2, 8, 2, 300, 300, 128, "bf16", seed=730)
+    o_p, l_p = run_host(q, k, v, "bf16")
+    o_u, l_u = run_host(q, k, v, "bf16", pinned=False)
+    assert np.array_equal(o_p, o_u) and np.array_equal(l_p, l_u)
+
+
+def test_two_threads_two_streams():
+    """Two host threads call fa_fwd_host at once on their own streams (the
+    library serialises its internal streams per device); both results equal
+    the single-threaded ones."""
+    import threading
+    shapes = [(2, 8, 2, 300, 300, 128, 740), (1, 6, 6, 500, 700, 64, 741)]
+    inputs = [I.make_general(B, H, Hk, Nq, Nk, d, "bf16", seed=sd) for B, H, Hk, Nq, Nk, d, sd in shapes]
+    ref = [run_host(q, k, v, "bf16") for q, k, v in inputs]
+    got = [None, None]
+    errors = []
+
+    def work(i):
+        try:
+            with torch.cuda.device(0):
+                s = torch.cuda.Stream()
+                got[i] = run_host(*inputs[i], "bf16", stream=s)
+        except Exception as exc:  # noqa: BLE001 - reported below
+            errors.append(exc)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not errors, errors
+    for (o_r, l_r), (o_g, l_g) in zip(ref, got):
+        assert np.array_equal(o_r, o_g) and np.array_equal(l_r, l_g)
 
 
 def test_without_lse_and_repeated():
