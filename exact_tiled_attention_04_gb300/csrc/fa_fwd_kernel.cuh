@@ -159,11 +159,36 @@ struct FwdCfg {
     static constexpr int kNumBars = kBarPVDone + 2;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
-    static constexpr int kSmemUsed = kOffAbort + 4;
+    static constexpr int kOffTurnFlags = kOffAbort + 4;  // [2][4] u32: turns each softmax warp has received
+    static constexpr int kSmemUsed = kOffTurnFlags + 32;
     static constexpr size_t kSmemBytes = static_cast<size_t>(kSmemUsed) + 1024;  // alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
     static_assert(kColO + 2 * D <= kTmemCols, "tensor memory budget exceeded");
 };
+
+// Bounded spin until *flag >= target, a shared counter that one warp of the
+// other softmax warpgroup advances; the same give-up rule as wait_phase.
+// (A spinning warp wakes within a few tens of clocks of the store, where an
+// mbarrier wait took about 150.)
+__device__ __forceinline__ bool wait_flag(volatile uint32_t* flag, uint32_t target,
+                                          volatile uint32_t* abort_flag, const FwdParams& fp,
+                                          unsigned int where) {
+    if (*flag >= target) return true;
+    const uint64_t t0 = global_timer_ns();
+    uint32_t spins = 0;
+    while (true) {
+        if (*flag >= target) return true;
+        if ((++spins & 31u) == 0u) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1u;
+                atomicOr(&fp.status->word, kDevErrTimeout | (where << 8));
+                atomicExch(&fp.status->abort_gen, fp.gen);
+                return false;
+            }
+        }
+    }
+}
 
 // Bounded wait on an mbarrier phase.  Returns false when the CTA is aborting
 // (if `honor_abort`) or when this wait itself gave up after kWaitLimitNs, in
@@ -542,6 +567,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(C::kBarQRaw), 1);
         for (int s = 0; s < C::kKStages; ++s) mbar_init(bar(C::kBarKRaw + s), 1);
         mbar_init(bar(C::kBarVRaw), 1);
+        {
+            // turn counters of the flag turns: warpgroup 0 holds the first turn
+            volatile uint32_t* tf = reinterpret_cast<volatile uint32_t*>(smem + C::kOffTurnFlags);
+            for (int i = 0; i < 8; ++i) tf[i] = i < 4 ? 1u : 0u;
+        }
         // A CTA starting after another CTA of this launch timed out does no work.
         *abort_flag = (*reinterpret_cast<volatile unsigned int*>(&p.status->abort_gen) == p.gen) ? 1u : 0u;
         mbar_init_fence();
@@ -760,15 +790,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Where they take turns (kTakeTurns), the two softmax warpgroups go
         // 0, 1, 0, 1, ...: one runs its exponentials while the other tile's
         // products occupy the tensor core (see kTurnAfterHalf for how far the
-        // turns overlap).
-        if (take_turns && w == 1 && lane == 0) mbar_arrive(bar(C::kBarTurn + 0));
+        // turns overlap).  Unmasked 16-bit launches pass the turn warp to
+        // warp (warp i of one warpgroup to warp i of the other, on the same
+        // scheduler) through shared counters the waiting warp spins on
+        // (+1 % on the headline shape); the others through mbarriers (the
+        // counters measured 1 % slower on the causal headline).
+        constexpr bool kFlagTurns = !TF32 && !kCausal;
+        volatile uint32_t* const turn_mine = reinterpret_cast<volatile uint32_t*>(smem + C::kOffTurnFlags) + 4 * w + wi;
+        volatile uint32_t* const turn_other =
+            reinterpret_cast<volatile uint32_t*>(smem + C::kOffTurnFlags) + 4 * (1 - w) + wi;
+        // hand the turn to the other warpgroup after this one's tile j
+        auto pass_turn = [&](int j) {
+            if (kFlagTurns) {
+                *turn_other = static_cast<uint32_t>(j + 1 + w);
+            } else {
+                mbar_arrive(bar(C::kBarTurn + (1 - w)));
+            }
+        };
+        if (!kFlagTurns && take_turns && w == 1 && lane == 0) mbar_arrive(bar(C::kBarTurn + 0));
         const int T_rows = active ? T : 0;
         for (int j = 0; j < T_rows; ++j) {  // T <= 0: no key tile
             bool got = wait_phase(bar(C::kBarSFull + w), j & 1, abort_flag, p, 10);
             ok = __all_sync(0xffffffffu, got);
             if (!ok) break;
             if (take_turns) {
-                got = wait_phase(bar(C::kBarTurn + w), j & 1, abort_flag, p, 13);
+                got = kFlagTurns ? wait_flag(turn_mine, static_cast<uint32_t>(j + 1), abort_flag, p, 13)
+                                 : wait_phase(bar(C::kBarTurn + w), j & 1, abort_flag, p, 13);
                 ok = __all_sync(0xffffffffu, got);
                 if (!ok) break;
             }
@@ -807,14 +854,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (q * 32 + i >= valid) s[q][i] = s[0][0];
             }
 
-            // Speculation (16-bit inputs at d = 64, unmasked tiles after the
-            // first): the first half's exponentials against the current
-            // reference run while the row maximum reduces.  When no row of
-            // the warp moves its reference (the lazy threshold below), they
-            // are exactly the values the path below would compute and are
-            // published as they are; otherwise that path recomputes them.
-            // (d = 64: +5 to +8 %; d = 128: no gain, not used.)
-            if constexpr (!TF32 && D == 64) {
+            // Speculation (16-bit inputs, unmasked tiles after the first; at
+            // d = 128 without the causal mask only): the first half's
+            // exponentials against the current reference run while the row
+            // maximum reduces.  When no row of the warp moves its reference
+            // (the lazy threshold below), they are exactly the values the
+            // path below would compute and are published as they are;
+            // otherwise that path recomputes them.  (d = 64: +5 to +8 %;
+            // d = 128: +1 % with the flag turns, -1 % on causal launches.)
+            if constexpr (!TF32 && (D == 64 || !kCausal)) {
                 if (!masked && j > 0) {
                     const float shift_s = (m_ref == -INFINITY) ? 0.0f : m_ref;
                     const uint64_t c2s = f2_pack(c, c);
@@ -834,13 +882,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar(C::kBarPFull + 2 * w + 0));
-                        if (take_turns && C::kTurnAfterHalf == 0 && lane == 0) mbar_arrive(bar(C::kBarTurn + (1 - w)));
+                        if (take_turns && C::kTurnAfterHalf == 0 && lane == 0) pass_turn(j);
                         exp_half<TF32, F16, false>(s, c2s, ns2s, valid, tP, 1, acc_s);
                         tmem_st_wait();
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(bar(C::kBarPFull + 2 * w + 1));
-                        if (take_turns && C::kTurnAfterHalf == 1 && lane == 0) mbar_arrive(bar(C::kBarTurn + (1 - w)));
+                        if (take_turns && C::kTurnAfterHalf == 1 && lane == 0) pass_turn(j);
                         const float tsum = sum8(acc_s);
                         const float pmax = ex2(fmaf(mx_s, c, -shift_s));
                         const float pmax_r = widen_lo16<F16>(pack_16x2<F16>(pmax, 0.0f));
@@ -913,7 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::kBarPFull + 2 * w + h));
-                if (take_turns && h == C::kTurnAfterHalf && lane == 0) mbar_arrive(bar(C::kBarTurn + (1 - w)));
+                if (take_turns && h == C::kTurnAfterHalf && lane == 0) pass_turn(j);
             }
             // l: fp32 sum of the weights (gives lse).  lq: the same sum with
             // the tile's largest weight replaced by its value as rounded for
