@@ -89,6 +89,40 @@ def reduce_sum(value: float, dist, device=None) -> float:
     return float(t.item())
 
 
+def rank_workload(w, rank: int):
+    """The workload a rank runs: the same shape with its own seed (weak
+    scaling, independent replicas: rank r draws its inputs from seed
+    w.seed + 17 r, so no two ranks compute the same problem)."""
+    return dataclasses.replace(w, seed=w.seed + 17 * rank)
+
+
+def aggregate(ms_local: float, flops_rank: float, dist, device=None):
+    """Whole-job figures from one rank's timed region: the slowest rank's
+    time (max over ranks) and every rank's work (sum), so value = all ranks'
+    flops / max-over-ranks time.  Returns (ms_total, flops_all, TFLOP/s)."""
+    ms_total = reduce_max(ms_local, dist, device)
+    flops_all = reduce_sum(flops_rank, dist, device)
+    return ms_total, flops_all, flops_all / (ms_total * 1e-3) / 1e12
+
+
+def result_line(w, world: int, steps: int, warmup: int, ms_total: float, value: float, *,
+                splits: int, launch: str, frac_of_peak, roofline: dict, e2e: dict,
+                gpu_launches: int, clocks: dict, entry: str) -> dict:
+    """The JSON line rank 0 prints for our arm (every rank's figures already
+    aggregated by `aggregate`)."""
+    return {
+        "metric": METRIC_BWD if w.backward else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": ms_total / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": dict(config_of(w, world, splits), launch=launch, entry_point=entry),
+        "frac_of_peak": frac_of_peak,
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+    }
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -357,7 +391,7 @@ def run_ours(args, w):
     fab.load()
 
     # per-rank inputs (weak scaling: every rank its own seeded copy)
-    wr = dataclasses.replace(w, seed=w.seed + 17 * rank)
+    wr = rank_workload(w, rank)
     q, k, v = I.make(wr)
 
     def host_tensor(x):
@@ -389,6 +423,7 @@ def run_ours(args, w):
         if st != fab.FA_OK:
             raise fab.FAError(st, "fa_fwd_ex")
 
+    entry_name = "fa_bwd" if w.backward else "fa_fwd_ex (num_splits = 0, caller workspace)"
     if not w.backward:
         # forward (+ merge of the partitions; + a split last wave with the automatic plan)
         kernels_per_step = fab.fa_fwd_ex_launches(w.B, w.H, w.H_kv, w.N, w.Nkv, w.d, dt_code, splits)
@@ -552,10 +587,7 @@ def run_ours(args, w):
         raise fab.FAError(st, "timed region")
     ms_local = (sum(e_a.elapsed_time(e_b) for e_a, e_b in step_events) if flush
                 else ev0.elapsed_time(ev1))
-    ms_total = reduce_max(ms_local, dist, dev)
-    flops_rank = w.flops() * args.steps
-    flops_all = reduce_sum(flops_rank, dist, dev)
-    value = flops_all / (ms_total * 1e-3) / 1e12
+    ms_total, _, value = aggregate(ms_local, w.flops() * args.steps, dist, dev)
     kernel_ms = ms_local / args.steps  # the step's kernels, all on this stream
     clk = clocks.summary()
 
@@ -586,8 +618,7 @@ def run_ours(args, w):
     torch.cuda.synchronize(dev)
     e2e_local = (sum(e_a.elapsed_time(e_b) for e_a, e_b in e2e_events) if flush
                  else e0.elapsed_time(e1))
-    e2e_ms = reduce_max(e2e_local, dist, dev)
-    e2e_value = reduce_sum(w.flops() * e2e_steps, dist, dev) / (e2e_ms * 1e-3) / 1e12
+    e2e_ms, _, e2e_value = aggregate(e2e_local, w.flops() * e2e_steps, dist, dev)
 
     if rank != 0:
         if dist is not None:
@@ -638,24 +669,18 @@ def run_ours(args, w):
                      "arithmetic_intensity": intensity})
     frac_tensor = value / world / tensor_peak
 
-    line = {
-        "metric": METRIC_BWD if w.backward else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_total / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": dict(config_of(w, world, splits),
-                       launch=(("K replays of a one-step CUDA graph" if step_graph is not None
-                                else "K plain launches") + ", each step bracketed by its own CUDA events"
-                               if flush else "one CUDA graph of the K steps" if graph is not None
-                               else "K plain launches")),
-        "frac_of_peak": frac_tensor,
-        "roofline": roofline,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
-        "gpu_launches": timed_launches,
-        "clocks": dict({k2: clk[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
-                       window=clock_window),
-    }
+    launch_text = (("K replays of a one-step CUDA graph" if step_graph is not None else "K plain launches")
+                   + ", each step bracketed by its own CUDA events" if flush
+                   else "one CUDA graph of the K steps" if graph is not None else "K plain launches")
+    line = result_line(
+        w, world, args.steps, args.warmup, ms_total, value, splits=splits, launch=launch_text,
+        frac_of_peak=frac_tensor, roofline=roofline,
+        e2e={"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+             "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
+        gpu_launches=timed_launches,
+        clocks=dict({k2: clk[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
+                    window=clock_window),
+        entry=entry_name)
     if world == 1 and not args.no_cpu_baseline:
         dout_np = I.make_dout(w.B, w.H, w.N, w.d, w.dtype, seed=wr.seed) if w.backward else None
         rate, cores, n, secs = cpu_oracle_rate(wr, q, k, v, dout_np, target_s=args.cpu_seconds)

@@ -54,10 +54,67 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 constexpr int kMaxDevices = 64;
-fa::DevStatus* g_err_ptr[kMaxDevices] = {};
 std::mutex g_err_mutex;
 std::atomic<unsigned int> g_generation{0};
+
+// Identity of the current CUDA context, unique over the process's life (the
+// driver's context id), or 0 when no context is current or the driver
+// entry points cannot be reached.  A device reset destroys the context and
+// the module's device symbols with it; the next context gets a new id.
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+unsigned long long current_context_id() {
+    std::call_once(g_ctx_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    });
+    if (g_ctx_current == nullptr || g_ctx_id == nullptr) return 0;
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    unsigned long long id = 0;
+    if (g_ctx_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
 }  // namespace
+
+// Device address of a __device__ variable of this library on the current
+// device, looked up once per device and context (cudaGetSymbolAddress, with
+// that device current) and looked up again after a device reset.  *status
+// gets FA_OK or FA_ERR_CUDA.
+void* SymbolCache::address(const void* symbol, const char* what, int* status) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxCachedDevices) {
+        set_error("cudaGetDevice", static_cast<int>(e), cudaGetErrorString(e));
+        *status = FA_ERR_CUDA;
+        return nullptr;
+    }
+    unsigned long long ctx = current_context_id();
+    std::lock_guard<std::mutex> lock(g_err_mutex);
+    if (ptr[dev] == nullptr || ctx == 0 || ctx != ctx_id[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, symbol);
+        if (e != cudaSuccess || p == nullptr) {
+            set_error(what, static_cast<int>(e), cudaGetErrorString(e));
+            *status = FA_ERR_CUDA;
+            return nullptr;
+        }
+        ptr[dev] = p;
+        ctx_id[dev] = current_context_id();  // the lookup made the context current if it was not
+    }
+    *status = FA_OK;
+    return ptr[dev];
+}
 
 // Launch generation: never 0 (0 is the status word's initial abort_gen).
 unsigned int next_generation() {
@@ -68,26 +125,9 @@ unsigned int next_generation() {
 
 // Device address of the status words on the current device.
 fa::DevStatus* device_status_words(int* status) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        set_error("cudaGetDevice", static_cast<int>(e), cudaGetErrorString(e));
-        *status = FA_ERR_CUDA;
-        return nullptr;
-    }
-    std::lock_guard<std::mutex> lock(g_err_mutex);
-    if (g_err_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_fa_device_status);
-        if (e != cudaSuccess) {
-            set_error("cudaGetSymbolAddress", static_cast<int>(e), cudaGetErrorString(e));
-            *status = FA_ERR_CUDA;
-            return nullptr;
-        }
-        g_err_ptr[dev] = static_cast<fa::DevStatus*>(p);
-    }
-    *status = FA_OK;
-    return g_err_ptr[dev];
+    static SymbolCache cache;
+    return static_cast<fa::DevStatus*>(
+        cache.address(&g_fa_device_status, "cudaGetSymbolAddress(status words)", status));
 }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -292,10 +332,11 @@ size_t auto_workspace_bound(int64_t B, int64_t H, int64_t N_q, int64_t d) {
     return r * (static_cast<size_t>(d) + 4) * sizeof(float);
 }
 
-int validate_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d,
-                float scale, int dtype_arg, int num_splits, const void* workspace,
-                size_t workspace_bytes) {
+// Every host check of fa_fwd_ex except those on the workspace: pointers,
+// sizes, dtype, alignment and overlaps of the tensors.
+int validate_args(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d,
+                  float scale, int dtype_arg, int num_splits) {
     if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || H_kv < 1 || N_q < 1 || N_kv < 1 || d < 1) return FA_ERR_INVALID_ARG;
     if (H % H_kv != 0) return FA_ERR_INVALID_ARG;
@@ -333,16 +374,41 @@ int validate_ex(const void* q, const void* k, const void* v, const void* o, cons
             overlaps(lse, lbytes, k, kvbytes) || overlaps(lse, lbytes, v, kvbytes))
             return FA_ERR_INVALID_ARG;
     }
-    const size_t need = make_launch_plan(B, H, H_kv, N_q, N_kv, d, dtype_arg, num_splits, device_sm_count()).workspace;
-    if (need > 0) {
-        if (workspace == nullptr || workspace_bytes < need) return FA_ERR_INVALID_ARG;
-        if (reinterpret_cast<uintptr_t>(workspace) & mask) return FA_ERR_ALIGNMENT;
-        if (overlaps(workspace, need, o, qbytes) || overlaps(workspace, need, q, qbytes) ||
-            overlaps(workspace, need, k, kvbytes) || overlaps(workspace, need, v, kvbytes) ||
-            (lse != nullptr && overlaps(workspace, need, lse, static_cast<size_t>(BH * N_q) * sizeof(float))))
-            return FA_ERR_INVALID_ARG;
-    }
     return FA_OK;
+}
+
+// Workspace bytes the plan of these (valid) arguments writes on the current device.
+size_t plan_workspace(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d,
+                      int dtype_arg, int num_splits) {
+    return make_launch_plan(B, H, H_kv, N_q, N_kv, d, dtype_arg, num_splits, device_sm_count()).workspace;
+}
+
+// The workspace checks of fa_fwd_ex for a plan that writes `need` bytes.
+int validate_workspace(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d,
+                       int dtype_arg, size_t need, const void* workspace, size_t workspace_bytes) {
+    if (need == 0) return FA_OK;
+    if (workspace == nullptr || workspace_bytes < need) return FA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) & 15) return FA_ERR_ALIGNMENT;
+    const int64_t elem = (dtype_arg & 0xFF) == FA_DTYPE_F32 ? 4 : 2;
+    const size_t qbytes = static_cast<size_t>(B * H * N_q * d * elem);
+    const size_t kvbytes = static_cast<size_t>(B * H_kv * N_kv * d * elem);
+    if (overlaps(workspace, need, o, qbytes) || overlaps(workspace, need, q, qbytes) ||
+        overlaps(workspace, need, k, kvbytes) || overlaps(workspace, need, v, kvbytes) ||
+        (lse != nullptr && overlaps(workspace, need, lse, static_cast<size_t>(B * H * N_q) * sizeof(float))))
+        return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
+
+int validate_ex(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d,
+                float scale, int dtype_arg, int num_splits, const void* workspace,
+                size_t workspace_bytes) {
+    const int st = validate_args(q, k, v, o, lse, B, H, H_kv, N_q, N_kv, d, scale, dtype_arg, num_splits);
+    if (st != FA_OK) return st;
+    const size_t need = plan_workspace(B, H, H_kv, N_q, N_kv, d, dtype_arg, num_splits);
+    return validate_workspace(q, k, v, o, lse, B, H, H_kv, N_q, N_kv, d, dtype_arg, need, workspace,
+                              workspace_bytes);
 }
 
 int launch_ex(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
@@ -567,33 +633,13 @@ namespace {
 constexpr size_t kStaticWorkspaceBytes = size_t(32) << 20;  // 32 MiB per device
 static __device__ __align__(256) unsigned char g_fa_static_workspace[kStaticWorkspaceBytes];
 
-void* g_static_ws[kMaxDevices] = {};
-std::mutex g_static_ws_mutex;
-
-// Device address of the static array on the current device, looked up once
-// per device (host code cannot use the array's name as a device address).
+// Device address of the static array on the current device, looked up with
+// cudaGetSymbolAddress the first time a device (or a new context of it,
+// after a device reset) uses it: host code cannot use the array's name as a
+// device address.
 void* static_workspace(int* status) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        set_error("cudaGetDevice", static_cast<int>(e), cudaGetErrorString(e));
-        *status = FA_ERR_CUDA;
-        return nullptr;
-    }
-    std::lock_guard<std::mutex> lock(g_static_ws_mutex);
-    if (g_static_ws[dev] == nullptr) {
-        void* ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_fa_static_workspace);
-        if (e != cudaSuccess || ptr == nullptr) {
-            set_error("cudaGetSymbolAddress(static workspace)", static_cast<int>(e),
-                      cudaGetErrorString(e));
-            *status = FA_ERR_CUDA;
-            return nullptr;
-        }
-        g_static_ws[dev] = ptr;
-    }
-    *status = FA_OK;
-    return g_static_ws[dev];
+    static SymbolCache cache;
+    return cache.address(&g_fa_static_workspace, "cudaGetSymbolAddress(static workspace)", status);
 }
 
 }  // namespace
@@ -605,29 +651,30 @@ size_t fa_fwd_ex_static_capacity(void) { return kStaticWorkspaceBytes; }
 int fa_fwd_ex_static(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
                      int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d, float scale,
                      int dtype, int num_splits, void* stream) {
+    // The worst case of the request must fit the array, whatever the device.
     if (B >= 1 && H >= 1 && N_q >= 1 && N_kv >= 1 && d >= 1 && num_splits >= 0) {
-        const size_t need = fa_fwd_ex_workspace_size(B, H, N_q, N_kv, d, num_splits);
-        if (need > kStaticWorkspaceBytes) {
+        const size_t bound = fa_fwd_ex_workspace_size(B, H, N_q, N_kv, d, num_splits);
+        if (bound > kStaticWorkspaceBytes) {
             std::snprintf(g_last_error, sizeof(g_last_error),
                           "fa_fwd_ex_static: the split partials need %zu bytes, more than the "
                           "%zu-byte static workspace; use fewer splits or fa_fwd_ex",
-                          need, kStaticWorkspaceBytes);
+                          bound, kStaticWorkspaceBytes);
             return FA_ERR_UNSUPPORTED;
         }
     }
-    // Host checks first.  A launch that keeps more than one partition fails
-    // them only for want of a workspace: check again with the static array
-    // once its device address is known.
-    int st = validate_ex(q, k, v, o, lse, B, H, H_kv, N_q, N_kv, d, scale, dtype, num_splits, nullptr,
-                         0);
+    // Every check that does not involve the workspace, before anything else.
+    int st = validate_args(q, k, v, o, lse, B, H, H_kv, N_q, N_kv, d, scale, dtype, num_splits);
+    if (st != FA_OK) return st;
+    const size_t need = plan_workspace(B, H, H_kv, N_q, N_kv, d, dtype, num_splits);
+    if (need > kStaticWorkspaceBytes) return FA_ERR_UNSUPPORTED;  // (the bound above covers it)
     void* ws = nullptr;
-    if (st == FA_ERR_INVALID_ARG && (num_splits > 1 || num_splits == 0)) {
+    if (need > 0) {
         ws = static_workspace(&st);
         if (st != FA_OK) return st;
-        st = validate_ex(q, k, v, o, lse, B, H, H_kv, N_q, N_kv, d, scale, dtype, num_splits, ws,
-                         kStaticWorkspaceBytes);
+        st = validate_workspace(q, k, v, o, lse, B, H, H_kv, N_q, N_kv, d, dtype, need, ws,
+                                kStaticWorkspaceBytes);
+        if (st != FA_OK) return st;
     }
-    if (st != FA_OK) return st;
     return launch_ex(q, k, v, o, lse, B, H, H_kv, N_q, N_kv, d, scale, dtype, num_splits, ws, stream);
 }
 

@@ -23,6 +23,17 @@ unsigned int next_generation();
 // FA_OK or FA_ERR_CUDA (with the error message set).
 DevStatus* device_status_words(int* status);
 
+// Per-device cache of one __device__ variable's address.  Entries are keyed
+// on the device's current CUDA context, so a device reset (which unloads the
+// module and may move the variable) is followed by a fresh lookup.
+constexpr int kMaxCachedDevices = 64;
+struct SymbolCache {
+    void* ptr[kMaxCachedDevices] = {};
+    unsigned long long ctx_id[kMaxCachedDevices] = {};
+    // `symbol`: the address of the variable as host code names it.
+    void* address(const void* symbol, const char* what, int* status);
+};
+
 // True when the byte ranges [a, a + na) and [b, b + nb) intersect.
 bool overlaps(const void* a, size_t na, const void* b, size_t nb);
 

@@ -307,6 +307,13 @@ size_t fa_bwd_workspace_size(int64_t B, int64_t H, int64_t N_q, int64_t d);
  * A launch that timed out leaves its outputs incomplete (the CTAs of that
  * launch stop early); later launches run normally whether or not the word
  * has been read.
+ *
+ * Source: "CUDA Flash Attention: Online Softmax with Shared Memory Tiling",
+ * Correctness Audit (13-Category Checklist), row "Async error surfacing"
+ * (the fused kernel's launch errors are checked with cudaGetLastError).  The
+ * page surfaces launch errors only; this call extends the same rule to
+ * errors a kernel detects while it runs, which an asynchronous launch cannot
+ * return.
  */
 int fa_device_status(void* stream);
 
@@ -320,7 +327,15 @@ int fa_device_status(void* stream);
  */
 int fa_selftest_barrier_timeout(void* stream);
 
-/* Static English text for a status code; never NULL. */
+/*
+ * Static English text for a status code; never NULL.
+ *
+ * Source: "CUDA Flash Attention: Online Softmax with Shared Memory Tiling",
+ * Correctness Audit (13-Category Checklist), rows "Async error surfacing"
+ * (cudaGetLastError after the launch) and "Latent coupling bugs" (the head
+ * dimension is checked, assert(d==64), instead of assumed).  Here those
+ * checks return status codes instead of aborting, and this call names them.
+ */
 const char* fa_status_string(int status);
 
 /* Text of the last CUDA error seen by this thread's calls ("" if none). */

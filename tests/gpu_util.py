@@ -63,6 +63,15 @@ def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
     return np.ldexp(1.0, e - 9)
 
 
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """float64 values rounded to the nearest bfloat16 (ties to even), as
+    float64: the best a bf16 output can be."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                   # x = m 2^e, |m| in [0.5, 1)
+    # 8 significant bits: m * 2^8 rounded to an integer (np.round: ties to even)
+    return np.ldexp(np.round(m * 256.0), e - 8)
+
+
 def half_ulp_f16(x: np.ndarray) -> np.ndarray:
     """Half an fp16 unit in the last place at |x| (11 significant bits)."""
     _, e = np.frexp(np.abs(x))
