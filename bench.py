@@ -355,6 +355,12 @@ def needs_flush(w) -> bool:
     return input_bytes(w) <= L2_BYTES
 
 
+def uses_fa_fwd(w) -> bool:
+    """Whether the benchmark's forward step calls fa_fwd (the workload fits
+    its signature and takes the automatic plan) rather than fa_fwd_ex."""
+    return w.H_kv == w.H and w.N == w.Nkv and w.splits == 0
+
+
 def config_of(w, n_gpus: int, splits: int = 1):
     what = "q,k,v,o,dO,lse" if w.backward else "q,k,v"
     nin = input_bytes(w)
@@ -370,7 +376,8 @@ def config_of(w, n_gpus: int, splits: int = 1):
     if w.causal:
         cfg["causal"] = True
     if splits == 0 and not w.backward:
-        cfg["splits"] = "automatic (fa_fwd_ex num_splits = 0: the library's plan for this GPU)"
+        cfg["splits"] = ("automatic: the library's plan for this GPU (key partitions of underfilled "
+                         "launches and of a partly filled last wave merged inside thread-block clusters)")
     elif splits > 1:
         cfg["splits"] = splits
     if w.backward:
@@ -416,17 +423,31 @@ def run_ours(args, w):
     work = torch.empty(max(wbytes, 16), dtype=torch.uint8, device=dev)  # caller-owned scratch
     launches = 0
 
+    # The forward step is fa_fwd, the library's primary entry point, wherever
+    # the workload fits its signature (one key/value head per query head,
+    # as many keys as queries, the automatic plan); grouped-head and decode
+    # workloads go through fa_fwd_ex with the automatic plan.
+    use_fa_fwd = uses_fa_fwd(w)
+
     def forward():
+        if use_fa_fwd:
+            st = fab.fa_fwd(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), do.data_ptr(), dlse.data_ptr(),
+                            w.B, w.H, w.N, w.d, scale, dt_code, sp)
+            if st != fab.FA_OK:
+                raise fab.FAError(st, "fa_fwd")
+            return
         st = fab.fa_fwd_ex(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), do.data_ptr(), dlse.data_ptr(),
                            w.B, w.H, w.H_kv, w.N, w.Nkv, w.d, scale, dt_code, splits,
                            work.data_ptr() if wbytes else None, wbytes, sp)
         if st != fab.FA_OK:
             raise fab.FAError(st, "fa_fwd_ex")
 
-    entry_name = "fa_bwd" if w.backward else "fa_fwd_ex (num_splits = 0, caller workspace)"
+    entry_name = ("fa_bwd" if w.backward else "fa_fwd" if use_fa_fwd
+                  else "fa_fwd_ex (num_splits = 0, caller workspace)")
     if not w.backward:
-        # forward (+ merge of the partitions; + a split last wave with the automatic plan)
-        kernels_per_step = fab.fa_fwd_ex_launches(w.B, w.H, w.H_kv, w.N, w.Nkv, w.d, dt_code, splits)
+        # the step's kernels: the forward kernel, plus a split last wave or a merge kernel
+        kernels_per_step = (fab.fa_fwd_launches(w.B, w.H, w.N, w.d, dt_code) if use_fa_fwd else
+                            fab.fa_fwd_ex_launches(w.B, w.H, w.H_kv, w.N, w.Nkv, w.d, dt_code, splits))
         step_fn = forward
         # end to end: fa_fwd_host on pinned host tensors (q, k, v up; o and
         # lse back, overlapped with the computation inside the call)
@@ -650,10 +671,20 @@ def run_ours(args, w):
         decode = w.dtype != "f32" and w.N * (w.H // w.H_kv) <= 32
         base = (f"{'fa_decode_kernel' if decode else 'fa_fwd_kernel'}"
                 f"<{w.dtype},{w.d}{',causal' if w.causal else ''}>")
-        if kernels_per_step == 3:
-            kernel_name = f"{base} (full waves) + {base} (last wave, split) + fa_merge_kernel"
+        if use_fa_fwd:
+            kernel_name = base if kernels_per_step == 1 else (
+                f"{base} (full waves) + {base} (last wave, keys split across the CTAs of a cluster)")
         else:
-            kernel_name = base + (" + fa_merge_kernel" if kernels_per_step == 2 else "")
+            # decode steps and packed grouped heads merge their partitions
+            # through the workspace; unpacked launches split only their last
+            # wave, in clusters
+            packed = w.H_kv < w.H and w.N * (w.H // w.H_kv) <= 128
+            if kernels_per_step == 1:
+                kernel_name = base
+            elif decode or packed:
+                kernel_name = f"{base} + fa_merge_kernel"
+            else:
+                kernel_name = f"{base} (full waves) + {base} (last wave, keys split across the CTAs of a cluster)"
     if intensity >= ridge:
         achieved = w.flops() / step_s / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": UNIT,

@@ -90,6 +90,8 @@ def load(path: str | None = None):
         lib.fa_fwd_ex_splits.argtypes = [i64, i64, i64, i64, i64, c_int]
         lib.fa_fwd_ex_launches.restype = c_int
         lib.fa_fwd_ex_launches.argtypes = [i64, i64, i64, i64, i64, i64, c_int, c_int]
+        lib.fa_fwd_launches.restype = c_int
+        lib.fa_fwd_launches.argtypes = [i64, i64, i64, i64, c_int]
         lib.fa_fwd_ex_static.restype = c_int
         lib.fa_fwd_ex_static.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, c_int,
                                          c_int, vp]
@@ -158,6 +160,10 @@ def fa_fwd_ex_splits(B: int, H: int, H_kv: int, N_q: int, N_kv: int, num_sms: in
 def fa_fwd_ex_launches(B: int, H: int, H_kv: int, N_q: int, N_kv: int, d: int, dtype: int,
                        num_splits: int) -> int:
     return load().fa_fwd_ex_launches(B, H, H_kv, N_q, N_kv, d, dtype, num_splits)
+
+
+def fa_fwd_launches(B: int, H: int, N: int, d: int, dtype: int) -> int:
+    return load().fa_fwd_launches(B, H, N, d, dtype)
 
 
 def fa_fwd_ex_static(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, H_kv: int,

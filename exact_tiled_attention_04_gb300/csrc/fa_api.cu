@@ -24,6 +24,12 @@
 // Set by the kernels when a bounded wait gives up (one per device).
 __device__ fa::DevStatus g_fa_device_status;
 
+namespace fa {
+// An empty kernel with the forward kernel's launch shape, used only to ask
+// the occupancy calculator about clusters (see device_shape); never launched.
+__global__ void fa_cluster_shape_probe() {}
+}  // namespace fa
+
 namespace {
 thread_local char g_last_error[512] = "";
 }  // namespace
@@ -246,46 +252,117 @@ size_t workspace_bytes_for(int64_t B, int64_t H, int64_t N_q, int64_t d, const S
     return static_cast<size_t>(sp.splits) * rows * (static_cast<size_t>(d) + 4) * sizeof(float);
 }
 
-// SM count of the current device (cached per device; 0 when the query
-// fails, which makes the automatic plan use one partition).
-int device_sm_count() {
-    static int cache[kMaxDevices] = {};
+// What the automatic plan needs to know about the current device: its SM
+// count, and how many thread-block clusters of s CTAs (one CTA per SM, as
+// every forward variant runs) can be resident at once.  The second depends
+// on how the SMs are grouped on the chip (on a 152-SM GB300: 76 clusters of
+// 2, 36 of 4, 15 of 8), so it is asked of the runtime.
+constexpr int kMaxClusterSplits = 8;  // portable cluster size
+
+struct DeviceShape {
+    int sms = 0;                                  // 0: no device answered
+    int max_clusters[kMaxClusterSplits + 1] = {};  // [s], s = 2 .. 8
+};
+
+DeviceShape query_device_shape(int dev) {
+    DeviceShape ds;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return ds;
+    ds.sms = n;
+    const int smem = 160 * 1024;  // above half an SM's shared memory: one CTA per SM
+    if (cudaFuncSetAttribute(fa::fa_cluster_shape_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return ds;
+    }
+    for (int cs = 2; cs <= kMaxClusterSplits; ++cs) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(cs));
+        cfg.blockDim = dim3(384);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int c = 0;
+        if (cudaOccupancyMaxActiveClusters(&c, fa::fa_cluster_shape_probe, &cfg) != cudaSuccess || c < 0) {
+            cudaGetLastError();
+            c = 0;  // unknown: no clusters of this size
+        }
+        ds.max_clusters[cs] = c;
+    }
+    return ds;
+}
+
+// The current device's shape (cached per device; sms = 0 when no device
+// answers, which makes the automatic plan use one partition).
+DeviceShape device_shape() {
+    static DeviceShape cache[kMaxDevices];
+    static bool known[kMaxDevices] = {};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DeviceShape{};
     std::lock_guard<std::mutex> lock(g_err_mutex);
-    if (cache[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) cache[dev] = n;
+    if (!known[dev]) {
+        cache[dev] = query_device_shape(dev);
+        known[dev] = cache[dev].sms > 0;
     }
     return cache[dev];
 }
 
+int device_sm_count() { return device_shape().sms; }
+
 // The launches of one fa_fwd_ex call.  num_splits >= 1: one launch with that
-// many key partitions (capped by plan_splits), merged when more than one.
+// many key partitions (capped by plan_splits), their partial results in the
+// caller's workspace, merged by a second kernel when more than one.
 // num_splits == 0 (automatic), on a GPU of `sms` SMs, one CTA per SM:
 //   * fewer query blocks than SMs: as many partitions as fill one wave
-//     (the fa_fwd_ex_splits count);
+//     (the fa_fwd_ex_splits count).  When they fit one thread-block cluster
+//     (at most 8, and every block's cluster resident at once) the
+//     partitions of a query block form a cluster and merge through
+//     distributed shared memory inside the same launch (no workspace, no
+//     merge kernel); the cluster is then made as large as the device can
+//     hold for this many blocks.  Otherwise (more partitions wanted,
+//     workspace allowed) they go through the workspace and the merge kernel.
 //   * several waves whose last one is at most half full (16-bit inputs,
-//     unmasked, one query head per query block, at least 32 key tiles per
-//     block): the full waves' blocks
-//     run unsplit, and the blocks of the last wave, which are the last in
-//     block order and so hold one contiguous range of output rows, run in a
-//     second launch split along the keys (at most 4 partitions, at most one
-//     wave of CTAs) and merged over that row range alone;
+//     unmasked, one query head per query block, at least kTailMinTiles key
+//     tiles per block): the full waves' blocks run unsplit, and the blocks of
+//     the last wave (the last in block order) run in a second launch, split
+//     along the keys into clusters of at most 4 partitions merged in-cluster;
 //   * otherwise one partition.
-// Either way the partial rows times partitions stay below sms x 256, which
-// bounds the workspace (fa_fwd_ex_workspace_size with num_splits == 0).
+// allow_workspace = false (fa_fwd): only in-cluster merges.  Any workspace a
+// plan uses stays below sms x 256 partial rows, which bounds
+// fa_fwd_ex_workspace_size with num_splits == 0.
+#ifndef FA_TAIL_MIN_TILES
+#define FA_TAIL_MIN_TILES 32
+#endif
+// the tail launch pays off when a block sweeps at least this many key tiles
+// (measured with the merge kernel: +10 % at 128 tiles, +1.2 % at 64, -1 % at 16)
+constexpr int kTailMinTiles = FA_TAIL_MIN_TILES;
+
 struct LaunchPlan {
     SplitPlan sp;              // partitions of the (first) launch
-    int64_t tail_first = -1;   // >= 0: first query block of the tail launch
+    bool cluster = false;      // the first launch merges its partitions in-cluster
+    int64_t tail_first = -1;   // >= 0: first query block of the tail launch (in-cluster merge)
     SplitPlan tail{};          // partitions of the tail launch
-    int64_t part_row0 = 0;     // tail launch: first output row of its partial slab
-    int64_t part_rows = 0;     // tail launch: rows of its slab
     size_t workspace = 0;      // bytes the plan writes
 };
 
+// Partitions of `items` query blocks that merge in-cluster: the largest count
+// <= limit (and <= kMaxClusterSplits) whose clusters can all be resident at
+// once; splits = 1 when none can.
+SplitPlan cluster_plan(int64_t N_kv, int64_t items, int limit, const DeviceShape& dev) {
+    for (int s = limit < kMaxClusterSplits ? limit : kMaxClusterSplits; s >= 2; --s) {
+        const SplitPlan sp = plan_splits(N_kv, s);
+        if (sp.splits >= 2 && items <= dev.max_clusters[sp.splits]) return sp;
+    }
+    return plan_splits(N_kv, 1);
+}
+
 LaunchPlan make_launch_plan(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d,
-                            int dtype_arg, int num_splits, int sms) {
+                            int dtype_arg, int num_splits, const DeviceShape& dev, bool allow_workspace) {
     LaunchPlan pl;
     if (num_splits >= 1) {
         pl.sp = plan_splits(N_kv, num_splits);
@@ -293,32 +370,39 @@ LaunchPlan make_launch_plan(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int
         return pl;
     }
     pl.sp = plan_splits(N_kv, 1);
+    const int sms = dev.sms;
     if (sms <= 0) return pl;
+    const int dtype = dtype_arg & 0xFF;
+    // the general kernel on unpacked query blocks merges in-cluster
+    const bool cluster_ok = !packed_heads(H, H_kv, N_q) && !(dtype != FA_DTYPE_F32 && decode_rows(H, H_kv, N_q));
     const int64_t blocks = ctas_per_partition(B, H, H_kv, N_q);
     if (blocks < sms) {
         const int64_t want = sms / blocks;
-        pl.sp = plan_splits(N_kv, static_cast<int>(want > kMaxSplits ? kMaxSplits : want));
-        pl.workspace = workspace_bytes_for(B, H, N_q, d, pl.sp);
+        const SplitPlan full = plan_splits(N_kv, static_cast<int>(want > kMaxSplits ? kMaxSplits : want));
+        if (full.splits < 2) return pl;
+        if (cluster_ok && (full.splits <= kMaxClusterSplits || !allow_workspace)) {
+            const SplitPlan cp = cluster_plan(N_kv, blocks, full.splits, dev);
+            if (cp.splits >= 2) {
+                pl.sp = cp;
+                pl.cluster = true;
+                return pl;
+            }
+        }
+        if (allow_workspace) {
+            pl.sp = full;
+            pl.workspace = workspace_bytes_for(B, H, N_q, d, pl.sp);
+        }
         return pl;
     }
-    const int dtype = dtype_arg & 0xFF;
-    const bool eligible = dtype != FA_DTYPE_F32 && !(dtype_arg & FA_FLAG_CAUSAL) &&
-                          !packed_heads(H, H_kv, N_q) && !decode_rows(H, H_kv, N_q);
+    const bool eligible = cluster_ok && dtype != FA_DTYPE_F32 && !(dtype_arg & FA_FLAG_CAUSAL) &&
+                          !packed_heads(H, H_kv, N_q);
     const int64_t frac = blocks % sms;  // blocks of the last wave
-    // the second launch and its merge cost a few microseconds: worth it only
-    // when the blocks sweep at least 32 key tiles (measured: +10 % at 128
-    // tiles, +1.2 % at 64, -1 % at 16)
-    if (!eligible || frac == 0 || 2 * frac > sms || pl.sp.n_kv_tiles < 32) return pl;
+    if (!eligible || frac == 0 || 2 * frac > sms || pl.sp.n_kv_tiles < kTailMinTiles) return pl;
     const int64_t ts = sms / frac < 4 ? sms / frac : 4;
-    const SplitPlan tail = plan_splits(N_kv, static_cast<int>(ts));
+    const SplitPlan tail = cluster_plan(N_kv, frac, static_cast<int>(ts), dev);
     if (tail.splits < 2) return pl;
     pl.tail = tail;
     pl.tail_first = blocks - frac;
-    const int64_t nqb = (N_q + 255) / 256;
-    pl.part_row0 = (pl.tail_first / nqb) * N_q + (pl.tail_first % nqb) * 256;
-    pl.part_rows = B * H * N_q - pl.part_row0;
-    pl.workspace = static_cast<size_t>(tail.splits) * static_cast<size_t>(pl.part_rows) *
-                   (static_cast<size_t>(d) + 4) * sizeof(float);
     return pl;
 }
 
@@ -380,7 +464,7 @@ int validate_args(const void* q, const void* k, const void* v, const void* o, co
 // Workspace bytes the plan of these (valid) arguments writes on the current device.
 size_t plan_workspace(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d,
                       int dtype_arg, int num_splits) {
-    return make_launch_plan(B, H, H_kv, N_q, N_kv, d, dtype_arg, num_splits, device_sm_count()).workspace;
+    return make_launch_plan(B, H, H_kv, N_q, N_kv, d, dtype_arg, num_splits, device_shape(), true).workspace;
 }
 
 // The workspace checks of fa_fwd_ex for a plan that writes `need` bytes.
@@ -411,13 +495,16 @@ int validate_ex(const void* q, const void* k, const void* v, const void* o, cons
                               workspace_bytes);
 }
 
+// allow_workspace: the plan may put split partials in `workspace` (fa_fwd_ex);
+// false for fa_fwd, which has none (its splits merge in-cluster).
 int launch_ex(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
               int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int64_t d, float scale,
-              int dtype_arg, int num_splits, void* workspace, void* stream) {
+              int dtype_arg, int num_splits, void* workspace, void* stream, bool allow_workspace = true) {
     const int dtype = dtype_arg & 0xFF;
     const bool causal = (dtype_arg & FA_FLAG_CAUSAL) != 0;
     const int64_t BH = B * H;
-    const LaunchPlan plan = make_launch_plan(B, H, H_kv, N_q, N_kv, d, dtype_arg, num_splits, device_sm_count());
+    const LaunchPlan plan =
+        make_launch_plan(B, H, H_kv, N_q, N_kv, d, dtype_arg, num_splits, device_shape(), allow_workspace);
     const SplitPlan sp = plan.sp;
     const bool pack = packed_heads(H, H_kv, N_q);
     const bool dec = dtype != FA_DTYPE_F32 && decode_rows(H, H_kv, N_q);
@@ -450,7 +537,9 @@ int launch_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
     const size_t rows = static_cast<size_t>(BH) * static_cast<size_t>(N_q);
     p.part_row0 = 0;
     p.part_rows = static_cast<long long>(rows);
-    if (sp.splits > 1) {
+    p.cluster = plan.cluster ? 1 : 0;
+    const bool via_workspace = sp.splits > 1 && !plan.cluster;
+    if (via_workspace) {
         p.o_part = static_cast<float*>(workspace);
         p.ml_part = p.o_part + static_cast<size_t>(sp.splits) * rows * static_cast<size_t>(d);
         p.lse = nullptr;
@@ -474,7 +563,7 @@ int launch_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
         return fa::launch_fwd_tf32_d64(mq, mk, mv, mo, lp, g, s);
     };
     cudaError_t e = launch(p, grid);
-    if (e == cudaSuccess && sp.splits > 1) {
+    if (e == cudaSuccess && via_workspace) {
         fa::MergeParams m{};
         m.o_part = p.o_part;
         m.ml_part = p.ml_part;
@@ -485,30 +574,18 @@ int launch_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
         e = fa::launch_merge(m, static_cast<int>(d), dtype, s);
     }
     if (e == cudaSuccess && plan.tail_first >= 0) {
-        // the last wave's blocks, split along the keys, merged over their rows
+        // the last wave's blocks, split along the keys into clusters that
+        // merge their partitions in distributed shared memory
         fa::FwdParams t = p;
         t.gen = next_generation();
         t.item_offset = static_cast<int>(plan.tail_first);
         t.splits = plan.tail.splits;
         t.tiles_per_split = plan.tail.tiles_per_split;
-        t.part_row0 = plan.part_row0;
-        t.part_rows = plan.part_rows;
-        t.o_part = static_cast<float*>(workspace);
-        t.ml_part = t.o_part + static_cast<size_t>(plan.tail.splits) * static_cast<size_t>(plan.part_rows) *
-                                   static_cast<size_t>(d);
-        t.lse = nullptr;
+        t.cluster = 1;
+        t.o_part = nullptr;
+        t.ml_part = nullptr;
+        t.lse = lse;
         e = launch(t, static_cast<unsigned int>((blocks - plan.tail_first) * plan.tail.splits));
-        if (e == cudaSuccess) {
-            const size_t elem = 2;  // 16-bit outputs (tail launches are 16-bit only)
-            fa::MergeParams m{};
-            m.o_part = t.o_part;
-            m.ml_part = t.ml_part;
-            m.o = static_cast<uint8_t*>(o) + static_cast<size_t>(plan.part_row0) * static_cast<size_t>(d) * elem;
-            m.lse = lse != nullptr ? lse + plan.part_row0 : nullptr;
-            m.rows = static_cast<long long>(plan.part_rows);
-            m.splits = plan.tail.splits;
-            e = fa::launch_merge(m, static_cast<int>(d), dtype, s);
-        }
     }
     if (e != cudaSuccess) {
         set_error("fa_fwd launch", static_cast<int>(e), cudaGetErrorString(e));
@@ -523,14 +600,22 @@ extern "C" {
 
 int fa_fwd_validate(const void* q, const void* k, const void* v, void* o, const float* lse,
                     int64_t B, int64_t H, int64_t N, int64_t d, float scale, int dtype) {
-    return validate_ex(q, k, v, o, lse, B, H, H, N, N, d, scale, dtype, 1, nullptr, 0);
+    return validate_args(q, k, v, o, lse, B, H, H, N, N, d, scale, dtype, 0);
 }
 
+// The automatic plan without a workspace: key partitions, where the device
+// is underfilled, merge inside thread-block clusters.
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
            int64_t N, int64_t d, float scale, int dtype, void* stream) {
-    const int st = validate_ex(q, k, v, o, lse, B, H, H, N, N, d, scale, dtype, 1, nullptr, 0);
+    const int st = validate_args(q, k, v, o, lse, B, H, H, N, N, d, scale, dtype, 0);
     if (st != FA_OK) return st;
-    return launch_ex(q, k, v, o, lse, B, H, H, N, N, d, scale, dtype, 1, nullptr, stream);
+    return launch_ex(q, k, v, o, lse, B, H, H, N, N, d, scale, dtype, 0, nullptr, stream, false);
+}
+
+int fa_fwd_launches(int64_t B, int64_t H, int64_t N, int64_t d, int dtype) {
+    if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+    const LaunchPlan pl = make_launch_plan(B, H, H, N, N, d, dtype, 0, device_shape(), false);
+    return pl.tail_first >= 0 ? 2 : 1;
 }
 
 int fa_fwd_ex_validate(const void* q, const void* k, const void* v, void* o, const float* lse,
@@ -562,9 +647,9 @@ int fa_fwd_ex_launches(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t 
                        int num_splits) {
     if (B < 1 || H < 1 || H_kv < 1 || H % H_kv != 0 || N_q < 1 || N_kv < 1 || d < 1 || num_splits < 0) return 0;
     const LaunchPlan pl = make_launch_plan(B, H, H_kv, N_q, N_kv, d, dtype, num_splits,
-                                           num_splits == 0 ? device_sm_count() : 0);
-    if (pl.tail_first >= 0) return 3;
-    return pl.sp.splits > 1 ? 2 : 1;
+                                           num_splits == 0 ? device_shape() : DeviceShape{}, true);
+    const int first = (pl.sp.splits > 1 && !pl.cluster) ? 2 : 1;  // + the merge kernel
+    return first + (pl.tail_first >= 0 ? 1 : 0);
 }
 
 int fa_fwd_ex_splits(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv, int num_sms) {

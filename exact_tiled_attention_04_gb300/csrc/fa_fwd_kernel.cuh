@@ -72,6 +72,7 @@ constexpr uint32_t kLaunchRegs = 168;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+constexpr int kMaxClusterParts = 8;  // key partitions merged in one cluster (portable size)
 
 template <bool TF32, int D, bool F16 = false>
 struct FwdCfg {
@@ -163,6 +164,12 @@ struct FwdCfg {
     static constexpr int kSmemUsed = kOffTurnFlags + 32;
     static constexpr size_t kSmemBytes = static_cast<size_t>(kSmemUsed) + 1024;  // alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget exceeded");
+    // In-cluster merge of split partials: the unnormalised O (256 rows x D
+    // fp32) and (m, l, lq) per row, written over the K and V rings once every
+    // product of the CTA has completed.
+    static constexpr int kOffPart = kOffK;
+    static_assert(256 * D * 4 <= kOffBar - kOffK, "partials do not fit the K/V rings");
+    static_assert(128 * 16 <= kTileBytes, "row statistics do not fit a query tile");
     static_assert(kColO + 2 * D <= kTmemCols, "tensor memory budget exceeded");
 };
 
@@ -315,11 +322,21 @@ __device__ __forceinline__ float sum8(const uint64_t (&a)[4]) {
 
 // Epilogue of one key partition of a split launch (one thread = one query
 // row): the unnormalised accumulator, relative to the reference maximum m,
-// and m, l, lq go to the partition's slab of the workspace.  Not inlined: it
-// runs once per CTA and keeps its address arithmetic out of the main loop.
+// and m, l, lq go to the partition's slab of the workspace (or, for an
+// in-cluster merge, m, l, lq to shared memory).  Not inlined: it runs once
+// per CTA, and keeping it a call keeps the softmax loop's register
+// allocation as it is (the same statistics stored inline there made ptxas
+// spill ten times more in the d = 128 kernel).
 template <int D>
 __device__ __noinline__ void store_partial(const FwdParams& p, uint32_t tO, long long qrow, float m_ref,
-                                           float l, float lq) {
+                                           float l, float lq, uint8_t* cluster_stats) {
+    if (p.cluster) {
+        // in-cluster merge: the row's statistics go to this CTA's shared
+        // memory (`cluster_stats`, in its query tile, whose products have all
+        // completed); O stays in tensor memory until cluster_merge
+        *reinterpret_cast<float4*>(cluster_stats) = make_float4(m_ref, l, lq, 0.0f);
+        return;
+    }
     // qrow: the query row's output row (of B*H*Nq), or -1 for a tile row
     // that is not a query row; a partition's slab holds rows part_row0 ..
     // part_row0 + part_rows - 1
@@ -475,6 +492,133 @@ __device__ void produce_tf32(const CUtensorMap& map_q, const CUtensorMap& map_k,
         }
         if (nv > 0) wait_phase(bar(C::kBarVRaw), (nv - 1) & 1, abort_flag, p, 25, false);
     }
+}
+
+// In-cluster merge of the key partitions of one 256-row query block (p.cluster):
+// the `splits` CTAs of a thread-block cluster swept disjoint key ranges of
+// the same query rows.  They combine like consecutive tiles of the online
+// softmax ("FlashAttention dissected", section "The mathematical
+// breakthrough: Tiling and Online Softmax": rescale by the correction factor
+// and add; section "Interaction with the KV cache during inference": the key
+// sequence split across cores), with M = max_s m_s, w_s = 2^(m_s - M):
+//   O = sum_s w_s O_s / sum_s w_s lq_s,   lse = ln 2 (M + log2 sum_s w_s l_s).
+// Run by all 384 threads of every CTA of the cluster, after every role has
+// finished (so every product has completed and every TMA load has landed),
+// on every path (the two cluster barriers need every thread of the cluster):
+//   1. the softmax threads have left each row's (m, l, lq) in their query
+//      tile's shared memory (free once that tile's products completed); here
+//      the warps copy the unnormalised O of both tiles out of tensor memory
+//      into shared memory, over the K/V rings (warp w reads TMEM lane
+//      quarter w % 4);
+//   2. cluster barrier;
+//   3. CTA r of the cluster reads rows [256 r / S, 256 (r + 1) / S) of every
+//      CTA's partials through distributed shared memory, combines them and
+//      writes O (input dtype) and lse to global memory, 8 columns per thread;
+//   4. cluster barrier (no CTA leaves while another still reads its memory).
+// `write`: the CTA's partials are valid (no role gave up on a wait).  The
+// code runs outside the role branches and holds nothing in registers across
+// them, so the softmax loop's register allocation does not see it.
+template <bool TF32, int D, bool F16>
+__device__ __forceinline__ void cluster_merge(const FwdParams& p, uint8_t* smem, uint32_t sbase, uint32_t tmem,
+                                              bool write, bool has_work, int row0, int bh) {
+    using C = FwdCfg<TF32, D, F16>;
+    const int warp = static_cast<int>(threadIdx.x) / 32;
+    const int lane = static_cast<int>(threadIdx.x) % 32;
+    if (write && has_work) {
+        uint8_t* part = smem + C::kOffPart;
+        const int quarter = warp % 4;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        // (tile, 32-column chunk) items of this lane quarter, dealt to its three warps
+        for (int item = warp / 4; item < 2 * (D / 32); item += 3) {
+            const int tile = item / (D / 32), q = item % (D / 32);
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_off + C::kColO + static_cast<uint32_t>(D * tile + 32 * q), o);
+            tmem_ld_wait(o);
+            const int r = 128 * tile + 32 * quarter + lane;  // row of the block
+            // 16-byte chunk c of row r at chunk position c ^ (r & 7): a warp's
+            // 32 rows then spread over all banks
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                const int c = 8 * q + ch;
+                *reinterpret_cast<uint4*>(part + r * D * 4 + ((c ^ (r & 7)) << 4)) =
+                    make_uint4(o[4 * ch], o[4 * ch + 1], o[4 * ch + 2], o[4 * ch + 3]);
+            }
+        }
+    }
+    cluster_sync_all();
+
+    const int S = p.splits;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int rb0 = (256 * rank) / S, rb1 = (256 * (rank + 1)) / S;
+    constexpr int kTpr = D / 8;  // threads per row (8 output columns each)
+    constexpr int kRowsPerPass = kThreads / kTpr;
+    const int i = static_cast<int>(threadIdx.x);
+    const int col0 = (i % kTpr) * 8;
+    const int c0 = col0 / 4;  // first of the two 16-byte chunks
+    const uint32_t part_s = sbase + C::kOffPart;
+    for (int rb = rb0 + i / kTpr; rb < rb1; rb += kRowsPerPass) {
+        const long long qi = static_cast<long long>(row0) + rb;
+        if (qi >= p.Nq) break;  // rows only grow along this loop
+        // row statistics of every partition: tile rb / 128, row rb % 128 of its Q tile
+        const uint32_t st_addr = sbase + C::kOffQ + (rb / 128) * C::kTileBytes + (rb % 128) * 16;
+        float ms[kMaxClusterParts], ls[kMaxClusterParts], lqs[kMaxClusterParts];
+        float M = -INFINITY;
+#pragma unroll
+        for (int s = 0; s < kMaxClusterParts; ++s) {
+            ms[s] = -INFINITY;
+            ls[s] = 0.0f;
+            lqs[s] = 0.0f;
+            if (s < S) {
+                const float4 st = ld_shared_cluster_f4(mapa_shared(st_addr, static_cast<uint32_t>(s)));
+                ms[s] = st.x;
+                ls[s] = st.y;
+                lqs[s] = st.z;
+                M = fmaxf(M, st.x);
+            }
+        }
+        const float mref = (M == -INFINITY) ? 0.0f : M;
+        float L = 0.0f, LQ = 0.0f;
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+        const uint32_t a0 = part_s + rb * D * 4 + ((c0 ^ (rb & 7)) << 4);
+        const uint32_t a1 = part_s + rb * D * 4 + (((c0 + 1) ^ (rb & 7)) << 4);
+#pragma unroll
+        for (int s = 0; s < kMaxClusterParts; ++s) {
+            const float wgt = (s < S) ? ex2(ms[s] - mref) : 0.0f;  // ex2(-inf) = 0: no visible key
+            L += wgt * ls[s];
+            LQ += wgt * lqs[s];
+            if (wgt != 0.0f) {  // a partition with no visible key wrote no O
+                const float4 x0 = ld_shared_cluster_f4(mapa_shared(a0, static_cast<uint32_t>(s)));
+                const float4 x1 = ld_shared_cluster_f4(mapa_shared(a1, static_cast<uint32_t>(s)));
+                acc[0] += wgt * x0.x;
+                acc[1] += wgt * x0.y;
+                acc[2] += wgt * x0.z;
+                acc[3] += wgt * x0.w;
+                acc[4] += wgt * x1.x;
+                acc[5] += wgt * x1.y;
+                acc[6] += wgt * x1.z;
+                acc[7] += wgt * x1.w;
+            }
+        }
+        const float inv = LQ > 0.0f ? 1.0f / LQ : 0.0f;
+        const size_t out_row = static_cast<size_t>(bh) * static_cast<size_t>(p.Nq) + static_cast<size_t>(qi);
+        if constexpr (TF32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + out_row * D + col0);
+            dst[0] = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+            dst[1] = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
+        } else {
+            uint4 v4;
+            v4.x = pack_16x2<F16>(acc[0] * inv, acc[1] * inv);
+            v4.y = pack_16x2<F16>(acc[2] * inv, acc[3] * inv);
+            v4.z = pack_16x2<F16>(acc[4] * inv, acc[5] * inv);
+            v4.w = pack_16x2<F16>(acc[6] * inv, acc[7] * inv);
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + out_row * D + col0) = v4;
+        }
+        if (p.lse != nullptr && col0 == 0)
+            p.lse[out_row] = (L > 0.0f) ? (mref + log2f(L)) * 0.69314718055994531f : -INFINITY;
+    }
+    cluster_sync_all();
 }
 
 // kOneTile: a packed launch (p.pack = 1), where query tile 1 holds no row;
@@ -750,6 +894,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_phase(bar(C::kBarDrain + w), 0, abort_flag, p, 9, false);
         }
       }
+        // The in-cluster merge after the role branches runs in every warp:
+        // back to the launch allocation first (this waits until the softmax
+        // warpgroups have returned theirs, which they do after their last
+        // wait).
+        if (!kOneTile && p.cluster) regs_increase<kLaunchRegs>();
     } else {
         // ------------------------------------------------ softmax warpgroups
         regs_increase<C::kSoftmaxRegs>();
@@ -985,7 +1134,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && split_mode && active) {
             tc_fence_after();
             if (has_work) {
-                store_partial<D>(p, tO, out_row, m_ref, l, lq);
+                store_partial<D>(p, tO, out_row, m_ref, l, lq, stage + t * 16);
+            } else if (!kOneTile && p.cluster) {
+                // no visible key: weight 0 in the in-cluster merge
+                *reinterpret_cast<float4*>(stage + t * 16) = make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
             } else if (out_row >= 0) {
                 // an empty partition: weight 0 in the merge (its O slot is not read)
                 const size_t r = split * static_cast<size_t>(p.part_rows) + static_cast<size_t>(out_row - p.part_row0);
@@ -1062,6 +1214,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        // back to the launch allocation for the in-cluster merge (see warpgroup 2)
+        if (!kOneTile && p.cluster) regs_decrease<kLaunchRegs>();
+    }
+
+    // ------------------------------------------------ in-cluster merge
+    if (!kOneTile && p.cluster) {
+        // every role is done: both tiles' products completed (the softmax
+        // warpgroups waited for them), every TMA load landed (the producer
+        // drained), and the row statistics are in shared memory
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        cluster_merge<TF32, D, F16>(p, smem, sbase, tmem, !skip && *abort_flag == 0u, has_work, row0, bh);
     }
 
     // --------------------------------------------------------------- teardown
@@ -1089,6 +1254,27 @@ cudaError_t launch_fwd_variant(const CUtensorMap& q, const CUtensorMap& k, const
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::kSmemBytes));
     if (e != cudaSuccess) return e;
+    if (p.cluster) {
+        // the p.splits partitions of a query block form one cluster
+        // (consecutive blockIdx.x, so a CTA's cluster rank is its partition)
+        if (kOneTile || p.splits < 2 || p.splits > 8 || grid % static_cast<unsigned>(p.splits) != 0)
+            return cudaErrorInvalidConfiguration;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr_cluster[1];
+        attr_cluster[0].id = cudaLaunchAttributeClusterDimension;
+        attr_cluster[0].val.clusterDim.x = static_cast<unsigned>(p.splits);
+        attr_cluster[0].val.clusterDim.y = 1;
+        attr_cluster[0].val.clusterDim.z = 1;
+        cfg.attrs = attr_cluster;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, q, k, v, o, p);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     kern<<<grid, kThreads, C::kSmemBytes, stream>>>(q, k, v, o, p);
     return cudaGetLastError();
 }

@@ -46,6 +46,10 @@ struct FwdParams {
                              // first block of a tail launch (see launch_ex)
     long long part_row0;     // splits > 1: output row of the first row of a partition's slab
     long long part_rows;     // splits > 1: rows of one partition's slab
+    int cluster;             // splits > 1 and 1 here: the partitions of a query block form
+                             // one thread-block cluster (of `splits` CTAs) and merge their
+                             // partial results through distributed shared memory; no
+                             // workspace (o_part, ml_part unused), O and lse written directly
 };
 
 // Merge of split partial results: O = sum_s w_s O_s / sum_s w_s lq_s,

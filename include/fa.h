@@ -72,15 +72,34 @@ typedef enum {
  * Ownership: the caller owns every buffer; the library allocates and frees
  * nothing on the device.  o and lse must not overlap the inputs or each other.
  *
+ * Work distribution (no workspace is needed): one CTA per 256 query rows of
+ * one (b, h).  When those CTAs underfill the GPU (fewer than one per SM),
+ * or the last of several waves is at most half full (16-bit inputs, no
+ * causal mask, N >= 4096), the affected query blocks split their keys into
+ * 2 to 8 partitions that run as one thread-block cluster and combine their
+ * partial results in distributed shared memory with the online-softmax
+ * rescaling ("FlashAttention dissected", sections "The mathematical
+ * breakthrough: Tiling and Online Softmax" and "Interaction with the KV
+ * cache during inference"); see fa_fwd_launches.  This is fa_fwd_ex's
+ * automatic plan (num_splits = 0) restricted to merges inside a cluster.
+ *
  * Errors: argument checks run on the host before any CUDA call and return
  * FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED / FA_ERR_ALIGNMENT without side
  * effects.  A failed launch returns FA_ERR_CUDA.  The call is asynchronous:
- * FA_OK means the kernel was enqueued; a kernel that aborted on a barrier
+ * FA_OK means the kernels were enqueued; a kernel that aborted on a barrier
  * timeout is reported by fa_device_status().  There is no CPU fallback.
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int64_t B, int64_t H, int64_t N, int64_t d, float scale, int dtype,
            void* stream);
+
+/*
+ * Kernel launches fa_fwd enqueues for these sizes on the current device: 1,
+ * or 2 when the last wave's query blocks run split in a second launch; 0 for
+ * invalid sizes.  The SM count and cluster occupancy of the current device
+ * are the CUDA queries here (without a device the plan is one launch).
+ */
+int fa_fwd_launches(int64_t B, int64_t H, int64_t N, int64_t d, int dtype);
 
 /*
  * fa_fwd_validate — the host-side argument checks of fa_fwd, alone.  Returns
@@ -112,12 +131,16 @@ int fa_fwd_validate(const void* q, const void* k, const void* v, void* o,
  *             count is capped at 32 and at one partition per 128 keys.
  *             0 chooses automatically for the current device (one CTA per
  *             SM): a launch with fewer query blocks than SMs gets the
- *             fa_fwd_ex_splits count; a launch of several waves whose
- *             last wave is at most half full (16-bit inputs, unmasked,
- *             query heads not packed, N_kv >= 4096) runs the full waves
- *             unsplit and the last wave's query blocks in a second launch
- *             split along the keys (up to 4 partitions), merged over their
- *             rows; otherwise one partition.
+ *             fa_fwd_ex_splits count, merged inside thread-block clusters
+ *             (distributed shared memory, no workspace, no merge kernel)
+ *             when at most 8 partitions are wanted and every query block's
+ *             cluster fits on the device at once, else through the
+ *             workspace and the merge kernel; a launch of several waves
+ *             whose last wave is at most half full (16-bit inputs,
+ *             unmasked, query heads not packed, N_kv >= 4096) runs the full
+ *             waves unsplit and the last wave's query blocks in a second
+ *             launch, split along the keys (up to 4 partitions) into
+ *             clusters that merge in-cluster; otherwise one partition.
  *   workspace, workspace_bytes: device scratch owned by the caller, 16-byte
  *             aligned, at least fa_fwd_ex_workspace_size(...) bytes; may be
  *             NULL when that size is 0.  Contents on entry do not matter.
@@ -163,9 +186,10 @@ int fa_fwd_ex_splits(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_
 
 /*
  * Kernel launches fa_fwd_ex enqueues for these arguments: 1 (one key
- * partition), 2 (partitions and their merge), or 3 (num_splits = 0 with a
- * split tail: the full waves, the tail's partitions, their merge); 0 for
- * invalid sizes.  For num_splits = 0 the plan is the current device's (the
+ * partition, or partitions merged in-cluster), 2 (partitions and their
+ * merge kernel, or num_splits = 0 with a split tail: the full waves, then
+ * the tail's clusters), 3 (partitions through the workspace, their merge and
+ * a tail launch; not produced by the current plan); 0 for invalid sizes.  For num_splits = 0 the plan is the current device's (the
  * SM-count query is the one CUDA call here).
  */
 int fa_fwd_ex_launches(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N_kv,
@@ -183,9 +207,11 @@ int fa_fwd_ex_launches(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t 
  *
  *   - Sizes whose partials exceed the capacity return FA_ERR_UNSUPPORTED
  *     (fa_fwd_ex_workspace_size() gives the bytes a call needs).
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *   - The first call on a device (and the first after a device reset)
+ *     looks up the array's device address (cudaGetSymbolAddress) with that
+ *     device current; make that first call before any stream capture.
+ *   - Plans that merge their partitions inside thread-block clusters (see
+ *     fa_fwd_ex, num_splits = 0) do not touch the array.
  *   - Every call on a device shares the array, which keeps the last call's
  *     contents (nothing in it needs to start at zero).  Calls whose kernels
  *     may overlap on the GPU race on it: serialise them.

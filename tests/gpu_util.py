@@ -45,7 +45,7 @@ def run_fa(w, q, k, v, scale=None, with_lse=True, stream=None):
     o = torch.full_like(tq, float("nan"))
     lse = torch.full((w.B, w.H, w.N), float("nan"), dtype=torch.float32, device="cuda") if with_lse else None
     s = stream if stream is not None else torch.cuda.current_stream()
-    dt = DTYPE_CODES[w.dtype]
+    dt = DTYPE_CODES[w.dtype] | (fab.FA_FLAG_CAUSAL if getattr(w, "causal", False) else 0)
     sc = float(w.scale if scale is None else scale)
     st = fab.fa_fwd(tq.data_ptr(), tk.data_ptr(), tv.data_ptr(), o.data_ptr(),
                     lse.data_ptr() if lse is not None else None,

@@ -147,6 +147,8 @@ def test_launch_counts(lib):
     assert fab.fa_fwd_ex_launches(1, 1, 1, 100, 100, 64, bf16, 4) == 1   # one key tile: no split
     # automatic plan without a device to ask: one partition
     assert fab.fa_fwd_ex_launches(2, 32, 32, 8192, 8192, 128, bf16, 0) == 1
+    assert fab.fa_fwd_launches(2, 32, 8192, 128, bf16) == 1
+    assert fab.fa_fwd_launches(0, 32, 8192, 128, bf16) == 0
     # invalid sizes
     assert fab.fa_fwd_ex_launches(1, 3, 2, 100, 100, 64, bf16, 1) == 0
     assert fab.fa_fwd_ex_launches(1, 1, 1, 100, 100, 64, bf16, -1) == 0

@@ -77,13 +77,17 @@ def test_split_matches_unsplit_closely():
     assert np.max(np.abs(o1 - o8)) <= 2 ** -7 and np.max(np.abs(l1 - l8)) <= 1e-4
 
 
-def test_fa_fwd_equals_fa_fwd_ex_unsplit():
+def test_fa_fwd_equals_fa_fwd_ex_automatic():
+    """fa_fwd is fa_fwd_ex's automatic plan where that plan merges in-cluster
+    (12 query blocks here: their keys split across clusters): the same bits."""
     w = I.custom(2, 3, 333, 128, "bf16", seed=93)
     q, k, v = I.make(w)
-    from .gpu_util import run_fa
+    from .gpu_util import compare, run_fa
     o_a, l_a = run_fa(w, q, k, v)
-    o_b, l_b = run_fa_ex(q, k, v, "bf16", 1)
+    o_b, l_b = run_fa_ex(q, k, v, "bf16", 0)
     assert np.array_equal(o_a, o_b) and np.array_equal(l_a, l_b)
+    err_o, err_l = compare(w, o_a, l_a, q, k, v)
+    assert err_o <= tol_o_dtype("bf16") and err_l <= TOL_LSE
 
 
 def test_workspace_too_small_is_rejected():
@@ -104,16 +108,21 @@ BENCH_FORWARD = [n for n, w in I.WORKLOADS.items() if not w.backward]
 
 @pytest.mark.parametrize("name", BENCH_FORWARD)
 def test_workloads_in_bench_launch_configuration(name):
-    """Every forward workload as the benchmark launches it: fa_fwd_ex with
-    the workload's num_splits (0: the library's plan for this device, which
-    on a 152-SM GPU splits the last wave of the headline shapes).  Every
-    output row must be written; the small workloads are compared on every
-    row, the large ones on seeded rows, the edge rows and rows of the last
-    three heads (the ones a split last wave covers)."""
-    from .gpu_util import edge_rows
+    """Every forward workload as the benchmark launches it: fa_fwd where the
+    workload fits its signature, else fa_fwd_ex with the workload's
+    num_splits (0: the library's plan for this device, which on a 152-SM GPU
+    splits the last wave of the headline shapes).  Every output row must be
+    written; the small workloads are compared on every row, the large ones on
+    seeded rows, the edge rows and rows of the last three heads (the ones a
+    split last wave covers)."""
+    from bench import uses_fa_fwd
+    from .gpu_util import edge_rows, run_fa
     w = I.WORKLOADS[name]
     q, k, v = I.make(w)
-    o, lse = run_fa_ex(q, k, v, w.dtype, w.splits, causal=w.causal)
+    if uses_fa_fwd(w):
+        o, lse = run_fa(w, q, k, v)
+    else:
+        o, lse = run_fa_ex(q, k, v, w.dtype, w.splits, causal=w.causal)
     assert np.isfinite(o).all() and np.isfinite(lse).all()
     rows = None
     if w.oracle_rows is not None:
@@ -161,18 +170,23 @@ def test_packed_causal_and_fp32():
 
 def test_automatic_plan_launch_counts():
     """The plan on this device: the headline shape on a 152-SM GPU runs its
-    13 full waves unsplit and its last 72 blocks split (3 launches); causal
-    and fp32 launches never take the split last wave; an underfilled launch
-    splits every block (2 launches)."""
+    13 full waves unsplit and its last 72 blocks in a second launch, split
+    into clusters that merge in distributed shared memory (2 launches);
+    causal and fp32 launches never take the split last wave; an underfilled
+    launch splits every block, merged in-cluster (1 launch) or, for the
+    decode kernel, through the workspace (2 launches)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     bf16, f32, causal = fab.FA_DTYPE_BF16, fab.FA_DTYPE_F32, fab.FA_FLAG_CAUSAL
     blocks = 2 * 32 * 32
     last = blocks % sms
-    expect = 3 if 0 < last and 2 * last <= sms else 1
+    expect = 2 if 0 < last and 2 * last <= sms else 1
     assert fab.fa_fwd_ex_launches(2, 32, 32, 8192, 8192, 128, bf16, 0) == expect
+    assert fab.fa_fwd_launches(2, 32, 8192, 128, bf16) == expect
     assert fab.fa_fwd_ex_launches(2, 32, 32, 8192, 8192, 128, bf16 | causal, 0) == 1
+    assert fab.fa_fwd_launches(2, 32, 8192, 128, bf16 | causal) == 1
     assert fab.fa_fwd_ex_launches(4, 16, 16, 2048, 2048, 64, bf16, 0) == 1   # 16 key tiles: not split
-    assert fab.fa_fwd_ex_launches(1, 1, 1, 512, 512, 64, f32, 0) == 2
+    assert fab.fa_fwd_ex_launches(1, 1, 1, 512, 512, 64, f32, 0) == 1       # clusters of 4
+    assert fab.fa_fwd_launches(1, 1, 512, 64, f32) == 1
     assert fab.fa_fwd_ex_launches(8, 32, 8, 1, 16384, 128, bf16, 0) == 2     # decode: 64 CTAs, 2 partitions
 
 
