@@ -351,9 +351,12 @@ struct LaunchPlan {
 };
 
 // Partitions of `items` query blocks that merge in-cluster: the largest count
-// <= limit (and <= kMaxClusterSplits) whose clusters can all be resident at
-// once; splits = 1 when none can.
-SplitPlan cluster_plan(int64_t N_kv, int64_t items, int limit, const DeviceShape& dev) {
+// <= limit (and <= what the kernel's shared memory can merge for this dtype
+// and head dimension) whose clusters can all be resident at once; splits = 1
+// when none can.
+SplitPlan cluster_plan(int64_t N_kv, int64_t items, int limit, const DeviceShape& dev, int dtype, int64_t d) {
+    const int cap = fa::fwd_max_merge_parts(dtype & 0xFF, static_cast<int>(d));
+    if (limit > cap) limit = cap;
     for (int s = limit < kMaxClusterSplits ? limit : kMaxClusterSplits; s >= 2; --s) {
         const SplitPlan sp = plan_splits(N_kv, s);
         if (sp.splits >= 2 && items <= dev.max_clusters[sp.splits]) return sp;
@@ -380,8 +383,8 @@ LaunchPlan make_launch_plan(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int
         const int64_t want = sms / blocks;
         const SplitPlan full = plan_splits(N_kv, static_cast<int>(want > kMaxSplits ? kMaxSplits : want));
         if (full.splits < 2) return pl;
-        if (cluster_ok && (full.splits <= kMaxClusterSplits || !allow_workspace)) {
-            const SplitPlan cp = cluster_plan(N_kv, blocks, full.splits, dev);
+        if (cluster_ok && (full.splits <= fa::fwd_max_merge_parts(dtype, static_cast<int>(d)) || !allow_workspace)) {
+            const SplitPlan cp = cluster_plan(N_kv, blocks, full.splits, dev, dtype, d);
             if (cp.splits >= 2) {
                 pl.sp = cp;
                 pl.cluster = true;
@@ -399,7 +402,7 @@ LaunchPlan make_launch_plan(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int
     const int64_t frac = blocks % sms;  // blocks of the last wave
     if (!eligible || frac == 0 || 2 * frac > sms || pl.sp.n_kv_tiles < kTailMinTiles) return pl;
     const int64_t ts = sms / frac < 4 ? sms / frac : 4;
-    const SplitPlan tail = cluster_plan(N_kv, frac, static_cast<int>(ts), dev);
+    const SplitPlan tail = cluster_plan(N_kv, frac, static_cast<int>(ts), dev, dtype, d);
     if (tail.splits < 2) return pl;
     pl.tail = tail;
     pl.tail_first = blocks - frac;

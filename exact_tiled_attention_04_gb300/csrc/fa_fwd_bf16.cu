@@ -1,4 +1,5 @@
 // bf16 instantiations of the forward kernel (head dimension 64 and 128).
+#include "fa.h"
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
@@ -21,6 +22,11 @@ __global__ void fa_selftest_wait_kernel(const FwdParams p) {
     __syncthreads();
 }
 
+
+int fwd_max_merge_parts(int dtype, int d) {
+    if (dtype == FA_DTYPE_F32) return d == 64 ? FwdCfg<true, 64>::kMaxMergeParts : 1;
+    return d == 64 ? FwdCfg<false, 64>::kMaxMergeParts : d == 128 ? FwdCfg<false, 128>::kMaxMergeParts : 1;
+}
 
 size_t fwd_smem_bytes_bf16_d64() { return FwdCfg<false, 64>::kSmemBytes; }
 size_t fwd_smem_bytes_bf16_d128() { return FwdCfg<false, 128>::kSmemBytes; }

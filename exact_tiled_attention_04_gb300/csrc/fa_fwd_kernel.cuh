@@ -15,9 +15,16 @@
 //   warps 0-3  softmax warpgroup 0: query tile 0 (rows 0-127 of the block)
 //   warps 4-7  softmax warpgroup 1: query tile 1 (rows 128-255)
 //   warp  8    tensor-core issuer of tile 0 (one thread) and TMEM owner
-//   warp  9    TMA producer (one thread; the whole warp for fp32 inputs)
+//   warp  9    TMA producer (one thread; the whole warp for fp32 inputs,
+//              which also rounds each K tile to TF32)
 //   warp 10    tensor-core issuer of tile 1 (one thread)
-//   warp 11    idle (completes warpgroup 2 for the register reallocation)
+//   warp 11    fp32 inputs: writes each V tile transposed (V^T, TF32);
+//              otherwise idle (completes warpgroup 2 for the register
+//              reallocation)
+// (fp32 inputs: the softmax warpgroups round their query tiles to TF32
+// before the first scores.)
+// Split launches whose partitions form a thread-block cluster merge them
+// after the roles finish, in every warp (cluster_merge).
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   S_w  columns [128w, 128w+128)   scores of tile w; P_w overwrites its
 //                                   first columns (bf16 pairs or tf32)
@@ -68,11 +75,11 @@ constexpr int kThreads = 384;
 constexpr int kMmaWarp = 8;   // tensor-core issuer of query tile 0, TMEM owner
 constexpr int kMmaWarp2 = 10; // tensor-core issuer of query tile 1
 constexpr int kLoadWarp = 9;
+constexpr int kTransposeWarp = 11;  // fp32 inputs: writes the V^T tiles (otherwise idle)
 constexpr uint32_t kLaunchRegs = 168;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;             // log2 units
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
-constexpr int kMaxClusterParts = 8;  // key partitions merged in one cluster (portable size)
 
 template <bool TF32, int D, bool F16 = false>
 struct FwdCfg {
@@ -157,7 +164,9 @@ struct FwdCfg {
     static constexpr int kBarTurn = kBarVRaw + 1;  // [2]: softmax warpgroup w may start a tile
     static constexpr int kBarSFree = kBarTurn + 2;   // [2] kEarlyS: S_w read (4 warps)
     static constexpr int kBarPVDone = kBarSFree + 2; // [2] kEarlyS: O_w += P_w V done
-    static constexpr int kNumBars = kBarPVDone + 2;
+    static constexpr int kBarVRawFree = kBarPVDone + 2;  // fp32 only: the raw V buffer was transposed
+    static constexpr int kBarMerge = kBarVRawFree + 1;    // in-cluster merge: the peers' rows landed
+    static constexpr int kNumBars = kBarMerge + 1;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kOffTurnFlags = kOffAbort + 4;  // [2][4] u32: turns each softmax warp has received
@@ -167,9 +176,23 @@ struct FwdCfg {
     // In-cluster merge of split partials: the unnormalised O (256 rows x D
     // fp32) and (m, l, lq) per row, written over the K and V rings once every
     // product of the CTA has completed.
-    static constexpr int kOffPart = kOffK;
-    static_assert(256 * D * 4 <= kOffBar - kOffK, "partials do not fit the K/V rings");
-    static_assert(128 * 16 <= kTileBytes, "row statistics do not fit a query tile");
+    // In-cluster merge (cluster_merge): a padded row per query row (D fp32,
+    // then m, l, lq, 0); the send buffer (256 rows) at the top of the operand
+    // area, the receive slots ((S - 1) x ceil(256 / S) rows) from its start.
+    static constexpr int kMergeRowBytes = D * 4 + 16;
+    static constexpr int kOffSend = kOffBar - 256 * kMergeRowBytes;
+    static_assert(kOffSend >= kOffQ + 2 * 2048, "send buffer over the row statistics");
+    static_assert(kOffSend % 16 == 0, "bulk copies need 16-byte alignment");
+    // the largest cluster whose receive slots fit below the send buffer
+    static constexpr int max_merge_parts() {
+        int s = 8;
+        while (s > 2 && (s - 1) * ((256 + s - 1) / s) * kMergeRowBytes > kOffSend - kOffQ) --s;
+        return s;
+    }
+    static constexpr int kMaxMergeParts = max_merge_parts();
+    static_assert((kMaxMergeParts - 1) * ((256 + kMaxMergeParts - 1) / kMaxMergeParts) * kMergeRowBytes <=
+                      kOffSend - kOffQ,
+                  "receive slots do not fit");
     static_assert(kColO + 2 * D <= kTmemCols, "tensor memory budget exceeded");
 };
 
@@ -372,48 +395,76 @@ __device__ __forceinline__ void zero_unloaded_q(uint8_t* q_tiles, int rows, int 
 }
 
 // Round `n16` 16-byte groups of fp32 in shared memory to TF32 in place
-// (round to nearest, ties away), one warp.
-__device__ __forceinline__ void round_tf32_inplace(uint8_t* base, int n16, int lane) {
-#pragma unroll 4
-    for (int i = lane; i < n16; i += 32) {
-        uint4* p4 = reinterpret_cast<uint4*>(base) + i;
-        uint4 v = *p4;
-        v.x = round_tf32(u2f(v.x));
-        v.y = round_tf32(u2f(v.y));
-        v.z = round_tf32(u2f(v.z));
-        v.w = round_tf32(u2f(v.w));
-        *p4 = v;
+// (round to nearest, ties away), by `nthreads` threads (thread `tid`).  The
+// loads of eight groups are issued before their stores, so their latencies
+// overlap.
+__device__ __forceinline__ void round_tf32_inplace(uint8_t* base, int n16, int tid, int nthreads) {
+    uint4* p4 = reinterpret_cast<uint4*>(base);
+    for (int i0 = tid; i0 < n16; i0 += 8 * nthreads) {
+        uint4 v[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+            if (i0 + b * nthreads < n16) v[b] = p4[i0 + b * nthreads];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            if (i0 + b * nthreads < n16) {
+                uint4 r;
+                r.x = round_tf32(u2f(v[b].x));
+                r.y = round_tf32(u2f(v[b].y));
+                r.z = round_tf32(u2f(v[b].z));
+                r.w = round_tf32(u2f(v[b].w));
+                p4[i0 + b * nthreads] = r;
+            }
+        }
     }
 }
 
 // fp32 V tile as loaded by TMA ([D/32 atoms][128 keys][128 bytes], swizzled)
 // -> TF32-rounded V^T in the K-major swizzled operand layout
-// ([4 atoms of 32 keys][D rows][128 bytes]).  Iteration i: lanes cover 32
-// consecutive d of one key group, so the reads are 4 row-contiguous 128-byte
-// lines and the 16-byte writes take the minimum 4 wavefronts.
+// ([4 atoms of 32 keys][D rows][128 bytes]), one warp.  Step i: lanes cover
+// 32 consecutive d of one group of four keys, so the reads are 4
+// row-contiguous 128-byte lines and the 16-byte writes take the minimum 4
+// wavefronts.  Eight steps' loads are issued before their stores (the two
+// buffers are distinct, which the compiler cannot see).
 template <int D>
 __device__ __forceinline__ void transpose_v_tf32(const uint8_t* vraw, uint8_t* vt, int lane) {
     constexpr int kDBlocks = D / 32;
-#pragma unroll 4
-    for (int i = 0; i < 32 * kDBlocks; ++i) {
-        const int d = (i % kDBlocks) * 32 + lane;
-        const int kg = i / kDBlocks;  // keys 4kg .. 4kg+3
-        const int atom_in = d / 32, c_in = (d % 32) / 4, w_in = (d % 4) * 4;
-        uint32_t r[4];
+    constexpr int kSteps = 32 * kDBlocks;
+    static_assert(kSteps % 8 == 0, "whole batches of steps");
+    for (int i0 = 0; i0 < kSteps; i0 += 8) {
+        uint32_t r[8][4];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int key = 4 * kg + t;
-            const uint8_t* src = vraw + atom_in * 16384 + key * 128 + ((c_in ^ (key & 7)) << 4) + w_in;
-            r[t] = round_tf32(*reinterpret_cast<const float*>(src));
+        for (int b = 0; b < 8; ++b) {
+            const int i = i0 + b;
+            const int d = (i % kDBlocks) * 32 + lane;
+            const int kg = i / kDBlocks;  // keys 4kg .. 4kg+3
+            const int atom_in = d / 32, c_in = (d % 32) / 4, w_in = (d % 4) * 4;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int key = 4 * kg + t;
+                r[b][t] = *reinterpret_cast<const uint32_t*>(vraw + atom_in * 16384 + key * 128 +
+                                                             ((c_in ^ (key & 7)) << 4) + w_in);
+            }
         }
-        uint8_t* dst = vt + (kg / 8) * (D * 128) + d * 128 + (((kg % 8) ^ (d & 7)) << 4);
-        *reinterpret_cast<uint4*>(dst) = make_uint4(r[0], r[1], r[2], r[3]);
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const int i = i0 + b;
+            const int d = (i % kDBlocks) * 32 + lane;
+            const int kg = i / kDBlocks;
+            uint8_t* dst = vt + (kg / 8) * (D * 128) + d * 128 + (((kg % 8) ^ (d & 7)) << 4);
+            *reinterpret_cast<uint4*>(dst) = make_uint4(round_tf32(u2f(r[b][0])), round_tf32(u2f(r[b][1])),
+                                                        round_tf32(u2f(r[b][2])), round_tf32(u2f(r[b][3])));
+        }
     }
 }
 
-// Producer warp of the fp32 (TF32) variant: TMA loads as in the bf16 path,
-// then the whole warp rounds Q and K tiles in place and writes V^T tiles,
-// each published on its own barrier after a proxy fence.
+// Producer warp of the fp32 (TF32) variant: TMA loads as in the 16-bit path
+// (Q, K and V land "raw" on their own barriers), then the whole warp rounds
+// each K tile in place and publishes it after a proxy fence.  The softmax
+// warpgroups round Q (they are idle until the first scores), and warp 11
+// writes the V^T tiles (transpose_tf32), so the three run side by side.  The
+// raw V buffer is single: the load of tile j waits until the transposer has
+// read tile j - 1 out of it.
 template <int D>
 __device__ void produce_tf32(const CUtensorMap& map_q, const CUtensorMap& map_k,
                              const CUtensorMap& map_v, const FwdParams& p, uint8_t* smem,
@@ -425,7 +476,6 @@ __device__ void produce_tf32(const CUtensorMap& map_q, const CUtensorMap& map_k,
     const uint64_t keep = policy_evict_last();
     const uint64_t once = policy_evict_first();
     int nk = 0, nv = 0;  // K and V tiles whose loads were issued
-    bool q_issued = false;
     bool ok = true;
     if (p.pack) zero_unloaded_q<C::kTileBytes, C::kAtoms, C::kAtomBytes>(smem + C::kOffQ, p.Nq * p.group, lane);
     if (lane == 0) {
@@ -442,17 +492,8 @@ __device__ void produce_tf32(const CUtensorMap& map_q, const CUtensorMap& map_k,
                                 bar(C::kBarQRaw), a * C::kAtomElems, row0 + w * kTileM, bh, once);
         }
     }
-    q_issued = true;
-    ok = all_ok(wait_phase(bar(C::kBarQRaw), 0, abort_flag, p, 20));
-    if (ok) {
-        round_tf32_inplace(smem + C::kOffQ, 2 * C::kTileBytes / 16, lane);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::kBarQFull));
-    }
     for (int j = 0; ok && j < T; ++j) {
         const int ks = j % C::kKStages;
-        const int vs = j % C::kVStages;
         ok = all_ok(wait_phase(bar(C::kBarKEmpty + ks), ((j / C::kKStages) & 1) ^ 1, abort_flag, p, 21));
         if (!ok) break;
         if (lane == 0) {
@@ -460,37 +501,60 @@ __device__ void produce_tf32(const CUtensorMap& map_q, const CUtensorMap& map_k,
             for (int a = 0; a < C::kAtoms; ++a)
                 tma_load_3d(sbase + C::kOffK + ks * C::kTileBytes + a * C::kAtomBytes, &map_k,
                             bar(C::kBarKRaw + ks), a * C::kAtomElems, (t_begin + j) * kTileN, kvh, keep);
-            // the raw V buffer was fully read by this warp's previous transpose
+        }
+        nk = j + 1;
+        // the raw V buffer is free once tile j - 1 was transposed out of it
+        if (j > 0) ok = all_ok(wait_phase(bar(C::kBarVRawFree), (j - 1) & 1, abort_flag, p, 24));
+        if (!ok) break;
+        if (lane == 0) {
             mbar_arrive_expect_tx(bar(C::kBarVRaw), C::kTileBytes);
             for (int a = 0; a < C::kAtoms; ++a)
                 tma_load_3d(sbase + C::kOffVRaw + a * C::kAtomBytes, &map_v, bar(C::kBarVRaw),
                             a * C::kAtomElems, (t_begin + j) * kTileN, kvh, keep);
         }
-        nk = j + 1;
         nv = j + 1;
         ok = all_ok(wait_phase(bar(C::kBarKRaw + ks), (j / C::kKStages) & 1, abort_flag, p, 22));
         if (!ok) break;
-        round_tf32_inplace(smem + C::kOffK + ks * C::kTileBytes, C::kTileBytes / 16, lane);
+        round_tf32_inplace(smem + C::kOffK + ks * C::kTileBytes, C::kTileBytes / 16, lane, 32);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::kBarKFull + ks));
-        ok = all_ok(wait_phase(bar(C::kBarVRaw), j & 1, abort_flag, p, 23));
-        if (!ok) break;
-        ok = all_ok(wait_phase(bar(C::kBarVEmpty + vs), ((j / C::kVStages) & 1) ^ 1, abort_flag, p, 24));
-        if (!ok) break;
-        transpose_v_tf32<D>(smem + C::kOffVRaw, smem + C::kOffV + vs * C::kTileBytes, lane);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::kBarVFull + vs));
     }
-    // Drain every TMA load this warp issued (see the bf16 producer).
+    // Drain every TMA load this warp issued (see the 16-bit producer).  At
+    // most one raw V load is in flight (each waits for the previous one's
+    // transpose), so the last issued one's phase is the one to wait for.
     if (lane == 0) {
-        if (q_issued) wait_phase(bar(C::kBarQRaw), 0, abort_flag, p, 25, false);
+        wait_phase(bar(C::kBarQRaw), 0, abort_flag, p, 25, false);
         for (int s = 0; s < C::kKStages && s < nk; ++s) {
             const int last = s + ((nk - 1 - s) / C::kKStages) * C::kKStages;
             wait_phase(bar(C::kBarKRaw + s), (last / C::kKStages) & 1, abort_flag, p, 25, false);
         }
         if (nv > 0) wait_phase(bar(C::kBarVRaw), (nv - 1) & 1, abort_flag, p, 25, false);
+    }
+}
+
+// Warp 11 of the fp32 variant: each raw V tile -> the V^T operand tile of
+// its stage (once the products of the tile that used the stage before have
+// completed), published after a proxy fence; then the raw buffer is handed
+// back to the producer.
+template <int D>
+__device__ void transpose_tf32(const FwdParams& p, uint8_t* smem, uint32_t sbase, int lane, int T,
+                               volatile uint32_t* abort_flag) {
+    using C = FwdCfg<true, D>;
+    auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * static_cast<uint32_t>(i); };
+    for (int j = 0; j < T; ++j) {
+        const int vs = j % C::kVStages;
+        if (!__all_sync(0xffffffffu, wait_phase(bar(C::kBarVRaw), j & 1, abort_flag, p, 23))) break;
+        if (!__all_sync(0xffffffffu, wait_phase(bar(C::kBarVEmpty + vs), ((j / C::kVStages) & 1) ^ 1, abort_flag, p,
+                                                26)))
+            break;
+        transpose_v_tf32<D>(smem + C::kOffVRaw, smem + C::kOffV + vs * C::kTileBytes, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(bar(C::kBarVFull + vs));
+            mbar_arrive(bar(C::kBarVRawFree));
+        }
     }
 }
 
@@ -502,95 +566,122 @@ __device__ void produce_tf32(const CUtensorMap& map_q, const CUtensorMap& map_k,
 // and add; section "Interaction with the KV cache during inference": the key
 // sequence split across cores), with M = max_s m_s, w_s = 2^(m_s - M):
 //   O = sum_s w_s O_s / sum_s w_s lq_s,   lse = ln 2 (M + log2 sum_s w_s l_s).
-// Run by all 384 threads of every CTA of the cluster, after every role has
-// finished (so every product has completed and every TMA load has landed),
-// on every path (the two cluster barriers need every thread of the cluster):
-//   1. the softmax threads have left each row's (m, l, lq) in their query
-//      tile's shared memory (free once that tile's products completed); here
-//      the warps copy the unnormalised O of both tiles out of tensor memory
-//      into shared memory, over the K/V rings (warp w reads TMEM lane
-//      quarter w % 4);
-//   2. cluster barrier;
-//   3. CTA r of the cluster reads rows [256 r / S, 256 (r + 1) / S) of every
-//      CTA's partials through distributed shared memory, combines them and
-//      writes O (input dtype) and lse to global memory, 8 columns per thread;
-//   4. cluster barrier (no CTA leaves while another still reads its memory).
-// `write`: the CTA's partials are valid (no role gave up on a wait).  The
-// code runs outside the role branches and holds nothing in registers across
-// them, so the softmax loop's register allocation does not see it.
+// CTA r of the cluster owns rows [256 r / S, 256 (r + 1) / S) of the block.
+// Distributed shared memory moves about 20 bytes per clock between two SMs
+// (measured: 64 KB in 3.3k clocks as one bulk copy, 4.2k as contiguous
+// 16-byte stores by the threads, 7.3k as stores scattered over rows), so the
+// rows travel as one bulk copy per peer.  Run by all 384 threads of every
+// CTA of the cluster, after every role has finished (every product has
+// completed and every TMA load has landed), on every path:
+//   1. stage: the warps copy this CTA's unnormalised O of both tiles out of
+//      tensor memory (warp w reads TMEM lane quarter w % 4) into a send
+//      buffer at the top of its shared memory, one padded row per query row
+//      (D fp32 and then (m, l, lq, 0), the statistics the softmax threads
+//      left in the query tiles), so each owner's rows are contiguous; and
+//      announce the bytes this CTA will receive on its merge barrier;
+//   2. cluster barrier: every CTA has staged and is done with its K/V rings,
+//      where the receive slots lie (a CTA whose partition sees no key gets
+//      here at once, and must not be written to while a peer still streams
+//      tiles);
+//   3. one thread sends each peer its rows in one bulk copy, into the peer's
+//      slot for this partition, completing on the peer's merge barrier;
+//   4. wait (bounded) for the peers' rows, combine the owned rows (own rows
+//      read from the send buffer) and write O (input dtype) and lse to global
+//      memory, 8 columns per thread;
+//   5. cluster barrier: every copy out of this CTA's send buffer has landed
+//      (each CTA passed step 4 only after its own copies arrived).
+// `write`: this CTA's partials are valid (no role gave up on a wait); a CTA
+// without valid partials still sends (meaningless rows of an already failed
+// launch), so no peer waits in vain.  The code runs outside the role
+// branches and holds nothing in registers across them, so the softmax
+// loop's register allocation does not see it.
 template <bool TF32, int D, bool F16>
 __device__ __forceinline__ void cluster_merge(const FwdParams& p, uint8_t* smem, uint32_t sbase, uint32_t tmem,
-                                              bool write, bool has_work, int row0, int bh) {
+                                              bool write, bool has_work, int row0, int bh,
+                                              volatile uint32_t* abort_flag) {
     using C = FwdCfg<TF32, D, F16>;
+    constexpr int kRowBytes = C::kMergeRowBytes;  // D fp32 + (m, l, lq, 0)
     const int warp = static_cast<int>(threadIdx.x) / 32;
     const int lane = static_cast<int>(threadIdx.x) % 32;
-    if (write && has_work) {
-        uint8_t* part = smem + C::kOffPart;
-        const int quarter = warp % 4;
-        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        // (tile, 32-column chunk) items of this lane quarter, dealt to its three warps
-        for (int item = warp / 4; item < 2 * (D / 32); item += 3) {
-            const int tile = item / (D / 32), q = item % (D / 32);
-            uint32_t o[32];
-            tmem_ld32(tmem + lane_off + C::kColO + static_cast<uint32_t>(D * tile + 32 * q), o);
-            tmem_ld_wait(o);
-            const int r = 128 * tile + 32 * quarter + lane;  // row of the block
-            // 16-byte chunk c of row r at chunk position c ^ (r & 7): a warp's
-            // 32 rows then spread over all banks
+    const int S = p.splits;
+    const int rmax = (256 + S - 1) / S;  // rows owned by one CTA, at most
+    const int me = static_cast<int>(cluster_ctarank());
+    const int rb0 = (256 * me) / S, rb1 = (256 * (me + 1)) / S;
+    // receive slots [S - 1][rmax rows] from the start of the Q tiles; the
+    // send buffer [256 rows] at the top of the operand area
+    uint8_t* recv = smem + C::kOffQ;
+    uint8_t* send = smem + C::kOffSend;
+    const uint32_t merge_bar = sbase + C::kOffBar + 8u * static_cast<uint32_t>(C::kBarMerge);
+
+    if (write) {
+        if (has_work) {
+            const int quarter = warp % 4;
+            const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+            // (tile, 32-column chunk) items of this lane quarter, dealt to its three warps
+            for (int item = warp / 4; item < 2 * (D / 32); item += 3) {
+                const int tile = item / (D / 32), q = item % (D / 32);
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + C::kColO + static_cast<uint32_t>(D * tile + 32 * q), o);
+                tmem_ld_wait(o);
+                // padded rows: a warp's 32 rows start 16 bytes apart in the
+                // banks, so its 16-byte stores take the minimum 4 wavefronts
+                uint4* dst = reinterpret_cast<uint4*>(send + (128 * tile + 32 * quarter + lane) * kRowBytes + 128 * q);
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const int c = 8 * q + ch;
-                *reinterpret_cast<uint4*>(part + r * D * 4 + ((c ^ (r & 7)) << 4)) =
-                    make_uint4(o[4 * ch], o[4 * ch + 1], o[4 * ch + 2], o[4 * ch + 3]);
+                for (int ch = 0; ch < 8; ++ch) dst[ch] = make_uint4(o[4 * ch], o[4 * ch + 1], o[4 * ch + 2], o[4 * ch + 3]);
             }
         }
+        if (threadIdx.x < 256) {
+            const int r = static_cast<int>(threadIdx.x);
+            *reinterpret_cast<uint4*>(send + r * kRowBytes + D * 4) =
+                *reinterpret_cast<const uint4*>(smem + C::kOffQ + (r / 128) * C::kTileBytes + (r % 128) * 16);
+        }
     }
+    if (threadIdx.x == 0)  // this CTA receives its owned rows from every peer
+        mbar_arrive_expect_tx(merge_bar, static_cast<uint32_t>((S - 1) * (rb1 - rb0) * kRowBytes));
+    fence_proxy_async_smem();  // the staged rows are read by the bulk copies
     cluster_sync_all();
 
-    const int S = p.splits;
-    const int rank = static_cast<int>(cluster_ctarank());
-    const int rb0 = (256 * rank) / S, rb1 = (256 * (rank + 1)) / S;
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < S; ++k) {
+            if (k == me) continue;
+            const int k0 = (256 * k) / S, k1 = (256 * (k + 1)) / S;
+            const int slot = me < k ? me : me - 1;  // the peer's slot for this partition
+            bulk_copy_to_peer(mapa_shared(sbase + C::kOffQ + static_cast<uint32_t>(slot * rmax * kRowBytes),
+                                          static_cast<uint32_t>(k)),
+                              smem_u32(send + k0 * kRowBytes), static_cast<uint32_t>((k1 - k0) * kRowBytes),
+                              mapa_shared(merge_bar, static_cast<uint32_t>(k)));
+        }
+    }
+    const bool arrived = __all_sync(0xffffffffu, wait_phase(merge_bar, 0, abort_flag, p, 17, false));
+
     constexpr int kTpr = D / 8;  // threads per row (8 output columns each)
     constexpr int kRowsPerPass = kThreads / kTpr;
     const int i = static_cast<int>(threadIdx.x);
     const int col0 = (i % kTpr) * 8;
-    const int c0 = col0 / 4;  // first of the two 16-byte chunks
-    const uint32_t part_s = sbase + C::kOffPart;
-    for (int rb = rb0 + i / kTpr; rb < rb1; rb += kRowsPerPass) {
+    for (int rb = rb0 + i / kTpr; arrived && rb < rb1; rb += kRowsPerPass) {
         const long long qi = static_cast<long long>(row0) + rb;
         if (qi >= p.Nq) break;  // rows only grow along this loop
-        // row statistics of every partition: tile rb / 128, row rb % 128 of its Q tile
-        const uint32_t st_addr = sbase + C::kOffQ + (rb / 128) * C::kTileBytes + (rb % 128) * 16;
-        float ms[kMaxClusterParts], ls[kMaxClusterParts], lqs[kMaxClusterParts];
+        const int rr = rb - rb0;
+        // partition s's row: this CTA's own in the send buffer, a peer's in its slot
+        auto row_of = [&](int s) -> const uint8_t* {
+            return s == me ? send + rb * kRowBytes : recv + ((s < me ? s : s - 1) * rmax + rr) * kRowBytes;
+        };
         float M = -INFINITY;
-#pragma unroll
-        for (int s = 0; s < kMaxClusterParts; ++s) {
-            ms[s] = -INFINITY;
-            ls[s] = 0.0f;
-            lqs[s] = 0.0f;
-            if (s < S) {
-                const float4 st = ld_shared_cluster_f4(mapa_shared(st_addr, static_cast<uint32_t>(s)));
-                ms[s] = st.x;
-                ls[s] = st.y;
-                lqs[s] = st.z;
-                M = fmaxf(M, st.x);
-            }
-        }
+        for (int s = 0; s < S; ++s) M = fmaxf(M, reinterpret_cast<const float4*>(row_of(s) + D * 4)->x);
         const float mref = (M == -INFINITY) ? 0.0f : M;
         float L = 0.0f, LQ = 0.0f;
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
-        const uint32_t a0 = part_s + rb * D * 4 + ((c0 ^ (rb & 7)) << 4);
-        const uint32_t a1 = part_s + rb * D * 4 + (((c0 + 1) ^ (rb & 7)) << 4);
-#pragma unroll
-        for (int s = 0; s < kMaxClusterParts; ++s) {
-            const float wgt = (s < S) ? ex2(ms[s] - mref) : 0.0f;  // ex2(-inf) = 0: no visible key
-            L += wgt * ls[s];
-            LQ += wgt * lqs[s];
-            if (wgt != 0.0f) {  // a partition with no visible key wrote no O
-                const float4 x0 = ld_shared_cluster_f4(mapa_shared(a0, static_cast<uint32_t>(s)));
-                const float4 x1 = ld_shared_cluster_f4(mapa_shared(a1, static_cast<uint32_t>(s)));
+        for (int s = 0; s < S; ++s) {
+            const uint8_t* row = row_of(s);
+            const float4 st = *reinterpret_cast<const float4*>(row + D * 4);
+            const float wgt = ex2(st.x - mref);  // ex2(-inf) = 0: no visible key
+            L += wgt * st.y;
+            LQ += wgt * st.z;
+            if (wgt != 0.0f) {  // a partition with no visible key staged no O
+                const float4 x0 = *reinterpret_cast<const float4*>(row + col0 * 4);
+                const float4 x1 = *reinterpret_cast<const float4*>(row + col0 * 4 + 16);
                 acc[0] += wgt * x0.x;
                 acc[1] += wgt * x0.y;
                 acc[2] += wgt * x0.z;
@@ -686,7 +777,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---------------------------------------------------------------- setup
     if (threadIdx.x == 0) {
-        mbar_init(bar(C::kBarQFull), 1);
+        // read first: its latency (a cold line at the start of a launch)
+        // overlaps the barrier setup below
+        const unsigned int abort_gen = *reinterpret_cast<volatile unsigned int*>(&p.status->abort_gen);
+        // fp32: the eight softmax warps round Q and arrive; else the TMA load
+        mbar_init(bar(C::kBarQFull), TF32 ? 8 : 1);
         const uint32_t issuers = one_tile ? 1u : 2u;
         for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(bar(C::kBarKFull + s), 1);
@@ -711,13 +806,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(C::kBarQRaw), 1);
         for (int s = 0; s < C::kKStages; ++s) mbar_init(bar(C::kBarKRaw + s), 1);
         mbar_init(bar(C::kBarVRaw), 1);
+        mbar_init(bar(C::kBarVRawFree), 1);
+        mbar_init(bar(C::kBarMerge), 1);
         {
             // turn counters of the flag turns: warpgroup 0 holds the first turn
             volatile uint32_t* tf = reinterpret_cast<volatile uint32_t*>(smem + C::kOffTurnFlags);
             for (int i = 0; i < 8; ++i) tf[i] = i < 4 ? 1u : 0u;
         }
         // A CTA starting after another CTA of this launch timed out does no work.
-        *abort_flag = (*reinterpret_cast<volatile unsigned int*>(&p.status->abort_gen) == p.gen) ? 1u : 0u;
+        *abort_flag = (abort_gen == p.gen) ? 1u : 0u;
         mbar_init_fence();
     }
     if (warp == kLoadWarp && lane == 0) {
@@ -797,6 +894,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wait_phase(bar(C::kBarVFull + s), (last / C::kVStages) & 1, abort_flag, p, 3, false);
             }
         }
+    } else if (warp == kTransposeWarp) {
+        // ------------------------------------------ fp32: V^T tiles (else idle)
+        if constexpr (TF32) transpose_tf32<D>(p, smem, sbase, lane, T, abort_flag);
     } else if (warp == kMmaWarp || warp == kMmaWarp2) {
         // ------------------------------------------------ tensor-core issuers
         // One issuing thread per query tile (warp 8: tile 0, warp 10: tile 1),
@@ -935,6 +1035,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         float lq = 0.0f;          // running sum used to normalise O: l with each
                                   // tile's largest weight as rounded for P V
         bool ok = true;
+
+        if constexpr (TF32) {
+            // fp32 inputs: this warpgroup rounds its query tile to TF32 in
+            // place (it is idle until the first scores); the issuers start
+            // once all eight softmax warps have arrived
+            if (has_work) {
+                ok = __all_sync(0xffffffffu, wait_phase(bar(C::kBarQRaw), 0, abort_flag, p, 16));
+                if (ok) {
+                    round_tf32_inplace(smem + C::kOffQ + w * C::kTileBytes, C::kTileBytes / 16, t, kTileM);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::kBarQFull));
+                }
+            }
+        }
 
         // Where they take turns (kTakeTurns), the two softmax warpgroups go
         // 0, 1, 0, 1, ...: one runs its exponentials while the other tile's
@@ -1226,7 +1341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        cluster_merge<TF32, D, F16>(p, smem, sbase, tmem, !skip && *abort_flag == 0u, has_work, row0, bh);
+        cluster_merge<TF32, D, F16>(p, smem, sbase, tmem, !skip && *abort_flag == 0u, has_work, row0, bh,
+                                    abort_flag);
     }
 
     // --------------------------------------------------------------- teardown
@@ -1257,7 +1373,7 @@ cudaError_t launch_fwd_variant(const CUtensorMap& q, const CUtensorMap& k, const
     if (p.cluster) {
         // the p.splits partitions of a query block form one cluster
         // (consecutive blockIdx.x, so a CTA's cluster rank is its partition)
-        if (kOneTile || p.splits < 2 || p.splits > 8 || grid % static_cast<unsigned>(p.splits) != 0)
+        if (kOneTile || p.splits < 2 || p.splits > C::kMaxMergeParts || grid % static_cast<unsigned>(p.splits) != 0)
             return cudaErrorInvalidConfiguration;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid);

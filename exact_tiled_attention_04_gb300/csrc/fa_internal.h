@@ -70,6 +70,11 @@ constexpr unsigned int kDevErrTimeout = 1u;
 // barrier phase nothing completes; it must give up and report a timeout.
 cudaError_t launch_selftest_wait(const FwdParams& p, cudaStream_t stream);
 
+// Largest thread-block cluster whose key partitions the forward kernel can
+// merge in shared memory, for a dtype (fa_dtype_t) and head dimension; 1 when
+// none.
+int fwd_max_merge_parts(int dtype, int d);
+
 // Shared memory a CTA of a variant needs (bytes, including alignment slack).
 size_t fwd_smem_bytes_bf16_d64();
 size_t fwd_smem_bytes_bf16_d128();

@@ -353,6 +353,19 @@ __device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
                  : "memory");
     return v;
 }
+__device__ __forceinline__ void st_shared_cluster_u4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
+// another CTA's of the cluster (`dst`, `bar`: shared::cluster addresses from
+// mapa), completing as transaction bytes on that CTA's mbarrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "r"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
 // One phase of the cluster-wide barrier: every thread of every CTA of the
 // cluster arrives (release: its earlier memory operations, shared memory
 // included, become visible) and waits for all (acquire).  Threads of a warp

@@ -51,12 +51,14 @@ def run_fwd(q, k, v, dtype, causal=False, scale=None):
 SHAPES = [
     (1, 1, 512, 64, "f32", False),     # 2 blocks, clusters of 4 (one key tile each)
     (1, 1, 129, 64, "bf16", False),    # 1 block, 2 partitions (the second sees one key)
-    (1, 1, 2048, 128, "bf16", False),  # 8 blocks, clusters of 8
+    (1, 1, 2048, 128, "bf16", False),  # 8 blocks, clusters of 3 (the d = 128 merge's limit)
     (1, 3, 1000, 64, "bf16", False),   # 12 blocks, clusters of 8, ragged keys and rows
     (2, 4, 1000, 64, "bf16", False),   # the tail-masking workload's shape: clusters of 4
-    (1, 2, 777, 128, "f16", True),     # causal: clusters of 7, partitions with no visible key
+    (1, 2, 777, 128, "f16", True),     # causal, clusters of 3, partitions with no visible key
     (1, 1, 700, 64, "f32", True),      # causal fp32, clusters of 6
     (1, 5, 300, 128, "bf16", False),   # 10 blocks, 3 key tiles: clusters of 3
+    (1, 1, 384, 64, "bf16", True),     # causal, clusters of 3: block 0's last partition
+    (1, 1, 384, 128, "bf16", True),    #   sees no key and finishes while its peers still run
 ]
 
 
