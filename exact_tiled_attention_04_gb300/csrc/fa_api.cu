@@ -336,10 +336,11 @@ int device_sm_count() { return device_shape().sms; }
 // plan uses stays below sms x 256 partial rows, which bounds
 // fa_fwd_ex_workspace_size with num_splits == 0.
 #ifndef FA_TAIL_MIN_TILES
-#define FA_TAIL_MIN_TILES 32
+#define FA_TAIL_MIN_TILES 16
 #endif
 // the tail launch pays off when a block sweeps at least this many key tiles
-// (measured with the merge kernel: +10 % at 128 tiles, +1.2 % at 64, -1 % at 16)
+// (measured with the merge kernel: +10 % at 128 tiles, +1.2 % at 64, -1 % at
+// 16; with the in-cluster merge +1 % at 16, b4h16_n2048 98.5 -> 97.4 us)
 constexpr int kTailMinTiles = FA_TAIL_MIN_TILES;
 
 struct LaunchPlan {

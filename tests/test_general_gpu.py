@@ -184,7 +184,9 @@ def test_automatic_plan_launch_counts():
     assert fab.fa_fwd_launches(2, 32, 8192, 128, bf16) == expect
     assert fab.fa_fwd_ex_launches(2, 32, 32, 8192, 8192, 128, bf16 | causal, 0) == 1
     assert fab.fa_fwd_launches(2, 32, 8192, 128, bf16 | causal) == 1
-    assert fab.fa_fwd_ex_launches(4, 16, 16, 2048, 2048, 64, bf16, 0) == 1   # 16 key tiles: not split
+    # 512 blocks of 16 key tiles: 3 full waves, a last wave of 56 split in clusters
+    assert fab.fa_fwd_ex_launches(4, 16, 16, 2048, 2048, 64, bf16, 0) == (2 if 0 < 512 % sms and 2 * (512 % sms) <= sms else 1)
+    assert fab.fa_fwd_ex_launches(8, 16, 16, 1024, 1024, 64, bf16, 0) == 1   # 8 key tiles: not split
     assert fab.fa_fwd_ex_launches(1, 1, 1, 512, 512, 64, f32, 0) == 1       # clusters of 4
     assert fab.fa_fwd_launches(1, 1, 512, 64, f32) == 1
     assert fab.fa_fwd_ex_launches(8, 32, 8, 1, 16384, 128, bf16, 0) == 2     # decode: 64 CTAs, 2 partitions
