@@ -115,3 +115,24 @@ def test_cluster_merge_deterministic_and_lse_optional():
     assert st == fab.FA_OK
     assert fab.fa_device_status(None) == fab.FA_OK
     assert np.array_equal(o1, o3.float().cpu().numpy())
+
+
+# (B, H, H_kv, N_q, N_kv, d, dtype, causal): fa_fwd_ex's automatic plan on
+# general shapes whose partitions merge in-cluster (query heads not packed)
+GENERAL = [
+    (1, 8, 2, 1000, 1000, 64, "bf16", False),   # grouped heads, 32 blocks, clusters of 4
+    (1, 10, 10, 500, 3000, 64, "bf16", False),  # N_q != N_kv, 20 blocks over 24 key tiles
+    (1, 24, 24, 500, 1200, 64, "bf16", True),   # causal with N_kv - N_q = 700, clusters of 3
+    (1, 4, 2, 700, 700, 64, "f32", False),      # fp32, grouped heads, 12 blocks
+]
+
+
+@pytest.mark.parametrize("B,H,H_kv,Nq,Nkv,d,dtype,causal", GENERAL)
+def test_automatic_plan_cluster_general_shapes(B, H, H_kv, Nq, Nkv, d, dtype, causal):
+    code = DTYPE_CODES[dtype] | (fab.FA_FLAG_CAUSAL if causal else 0)
+    assert fab.fa_fwd_ex_launches(B, H, H_kv, Nq, Nkv, d, code, 0) == 1  # merged in-cluster
+    q, k, v = I.make_general(B, H, H_kv, Nq, Nkv, d, dtype, seed=760 + H + Nq)
+    o, lse = run_fa_ex(q, k, v, dtype, 0, causal=causal)
+    assert np.isfinite(o).all()
+    err_o, err_l = compare_ex(dtype, o, lse, q, k, v, causal=causal)
+    assert err_o <= tol_o_dtype(dtype) and err_l <= TOL_LSE, (err_o, err_l)
