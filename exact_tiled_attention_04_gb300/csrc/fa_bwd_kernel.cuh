@@ -18,6 +18,7 @@
 //   warp 10    dQ reducer (one thread): TMA tensor reductions of the
 //              staged dQ into the fp32 accumulator
 //   warp 11    idle (completes warpgroup 2 for the register reallocation)
+//   warps 12-15 (read-out layout only) dQ read-out warpgroup
 // Each thread of a gradient warpgroup owns one key row (its TMEM lane) and
 // half of the query columns.  The scores are computed transposed (keys on
 // the lanes) so that dK and dV accumulate in tensor memory for the whole
@@ -43,6 +44,19 @@
 // lines); the stage goes back to the producer when both reductions have read
 // it.  A last kernel scales and converts the accumulator.
 //
+// Read-out layout (d = 128 without the causal mask; 512 threads): warps
+// 12-15 form a fourth warpgroup that reads each tile's dQ out of tensor
+// memory, one query row a thread, so the gradient warpgroups go straight
+// from dS(j) to P^T(j+1).  The issuer then enqueues dQ(j) before dK(j), and
+// the next tile's scores after both (issued earlier they would wait in
+// front of dQ(j) for the next Q tile, whose stage is still being reduced
+// from).  The read-out warpgroup stages dQ columns [d/2, d) in the dO tile
+// as soon as dQ(j) is computed (dV(j) ran before it) and [0, d/2) in the
+// Q tile once dK(j) is; the reducer adds each half as soon as it is staged.
+// With the causal mask (short sweeps, where a CTA's fixed cost weighs
+// more) and at d = 64 (dQ in its own columns, so the next scores go early)
+// the 384-thread layout measured faster.
+//
 // Shared memory (128-byte-swizzled TMA tiles, 1024-byte aligned): K and V of
 // the key block (reused as the dK / dV output staging), a two-stage ring of
 // Q, dO and row-statistics tiles, and dS (128 keys x 128 queries, the
@@ -62,16 +76,22 @@
 
 namespace fa {
 
-constexpr int kBwdThreads = 384;
 constexpr int kBwdMmaWarp = 8;
 constexpr int kBwdLoadWarp = 9;
 constexpr int kBwdReduceWarp = 10;
-constexpr uint32_t kBwdLaunchRegs = 168;
+constexpr int kBwdReadWarp0 = 12;  // read-out layout: first warp of the dQ read-out warpgroup
 constexpr uint32_t kBwdTmemCols = 512;
 constexpr uint64_t kBwdWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 constexpr int kBwdStatBytes = kStatFloatsPerTile * static_cast<int>(sizeof(float));  // one query tile
 
-template <int D, bool F16>
+// The read-out layout (a dQ read-out warpgroup of its own) for d = 128
+// without the causal mask; the 384-thread layout otherwise.
+template <int D, bool kCausal>
+constexpr bool bwd_read_layout() {
+    return D == 128 && !kCausal;
+}
+
+template <int D, bool F16, bool kRead>
 struct BwdCfg {
     static constexpr int kAtomElems = 64;                // 16-bit elements per 128-byte row
     static constexpr int kAtoms = D / kAtomElems;
@@ -93,10 +113,13 @@ struct BwdCfg {
     // B = K ([keys x d]) MN-major; M = 128 query rows.
     static constexpr uint32_t kIdescDQ = instr_desc(kFmt, true, true, 128, D);
 
-    // register split (setmaxnreg): gradient warpgroups / warpgroup 2
-    static constexpr uint32_t kGradRegs = 208;
-    static constexpr uint32_t kOtherRegs = 88;
-    static_assert(2 * 128 * kGradRegs + 128 * kOtherRegs == kBwdThreads * kBwdLaunchRegs,
+    static constexpr int kThreads = kRead ? 512 : 384;
+    static constexpr uint32_t kLaunchRegs = kRead ? 128 : 168;
+    // register split (setmaxnreg): gradient warpgroups / warpgroup 2 / read-out warpgroup
+    static constexpr uint32_t kGradRegs = kRead ? 160 : 208;
+    static constexpr uint32_t kOtherRegs = kRead ? 96 : 88;
+    static constexpr uint32_t kReadRegs = kRead ? 96 : 0;
+    static_assert(2 * 128 * kGradRegs + 128 * kOtherRegs + 128 * kReadRegs == kThreads * kLaunchRegs,
                   "register split must equal the launch allocation");
 
     // shared-memory map (offsets from the 1024-aligned base)
@@ -122,12 +145,16 @@ struct BwdCfg {
     static constexpr int kBarP = kBarDP + 1;           // P^T in TMEM (8 warp arrivals)
     static constexpr int kBarDS = kBarP + 1;           // dS^T in TMEM and dS in smem (8)
     static constexpr int kBarDQ = kBarDS + 1;          // dQ computed
-    static constexpr int kBarDQFree = kBarDQ + 1;      // dQ read out (8)
+    static constexpr int kBarDK = kBarDQ + 1;          // read-out layout: dK computed, the Q tile read
+    static constexpr int kBarDQFree = kBarDK + 1;      // dQ read out (8; read-out layout 4)
     static constexpr int kBarAcc = kBarDQFree + 1;     // dK, dV final
     static constexpr int kBarDrain = kBarAcc + 1;
     static constexpr int kBarEpi = kBarDrain + 1;      // [2]
-    static constexpr int kBarStaged = kBarEpi + 2;     // [kStages]: the tile's dQ is staged (8)
-    static constexpr int kNumBars = kBarStaged + kStages;
+    // [kStages]: the tile's dQ is staged (8); read-out layout: its columns
+    // [0, d/2), in the Q tile (4)
+    static constexpr int kBarStaged = kBarEpi + 2;
+    static constexpr int kBarStagedDO = kBarStaged + kStages;  // [kStages] read-out layout: [d/2, d), in the dO tile (4)
+    static constexpr int kNumBars = kBarStagedDO + kStages;
     // barriers, TMEM slot and abort flag
     static constexpr int kCtrlBytes = kNumBars * 8 + 8;
     // The control block lives in whichever alignment gap holds it: below the
@@ -211,13 +238,34 @@ __device__ __forceinline__ void bulk_wait_read() {
 
 __device__ __forceinline__ float bwd_u2f(uint32_t x) { return __uint_as_float(x); }
 
+// 32 lanes x 16 consecutive fp32 columns of tensor memory, and the wait for
+// them (the registers tied so that no use is scheduled before it).
+__device__ __forceinline__ void bwd_tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void bwd_tmem_ld_wait16(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+
 template <int D, bool F16, bool kCausal>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__((BwdCfg<D, F16, bwd_read_layout<D, kCausal>()>::kThreads), 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                   const __grid_constant__ CUtensorMap map_dk, const __grid_constant__ CUtensorMap map_dv,
                   const __grid_constant__ CUtensorMap map_dq, const BwdParams p) {
-    using C = BwdCfg<D, F16>;
+    constexpr bool kRead = bwd_read_layout<D, kCausal>();
+    using C = BwdCfg<D, F16, kRead>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_u32 & 1023u)) & 1023u;
@@ -267,14 +315,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(bar(C::kBarFullDO + s), 1);
             mbar_init(bar(C::kBarEmpty + s), 1);
             mbar_init(bar(C::kBarEmptyDO + s), 1);
-            mbar_init(bar(C::kBarStaged + s), 8);
+            mbar_init(bar(C::kBarStaged + s), kRead ? 4 : 8);
+            mbar_init(bar(C::kBarStagedDO + s), 4);
         }
         mbar_init(bar(C::kBarS), 1);
         mbar_init(bar(C::kBarDP), 1);
         mbar_init(bar(C::kBarP), 8);  // one arrival per gradient warp
         mbar_init(bar(C::kBarDS), 8);
         mbar_init(bar(C::kBarDQ), 1);
-        mbar_init(bar(C::kBarDQFree), 8);
+        mbar_init(bar(C::kBarDK), 1);
+        mbar_init(bar(C::kBarDQFree), kRead ? 4 : 8);
         mbar_init(bar(C::kBarAcc), 1);
         mbar_init(bar(C::kBarDrain), 1);
         mbar_init(bar(C::kBarEpi + 0), 128);
@@ -302,6 +352,54 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (skip) {
         // nothing issued: go straight to the teardown
+    } else if (kRead && warp >= kBwdReadWarp0) {
+        // ------------------------------ dQ read-out warpgroup (read-out layout)
+        // Tile j's dQ (query row t, all d columns): columns [d/2, d) into the
+        // stage's dO tile once dQ(j) is computed (dV(j), the tile's last
+        // reader, ran before it), then [0, d/2) into its Q tile once dK(j)
+        // has read it; fp32 boxes of 32 columns with the 128-byte swizzle,
+        // the layout the reducer's tensor reductions read.
+        regs_decrease<C::kReadRegs>();
+        const int wi = warp % 4;        // TMEM lane quarter this warp may access
+        const int t = wi * 32 + lane;   // query row of the tile (= TMEM lane)
+        const uint32_t tDQ = tmem + (static_cast<uint32_t>(wi * 32) << 16) + C::kColDQ;
+        for (int it = 0; it < T; ++it) {
+            const int s = it % C::kStages;
+            bool got = bwd_wait(bar(C::kBarDQ), it & 1, abort_flag, p, 46);
+            if (!__all_sync(0xffffffffu, got)) break;
+            tc_fence_after();
+            bool fine = true;
+#pragma unroll
+            for (int half = 1; half >= 0; --half) {
+                if (half == 0) {
+                    got = bwd_wait(bar(C::kBarDK), it & 1, abort_flag, p, 47);
+                    fine = __all_sync(0xffffffffu, got);
+                    if (!fine) break;
+                }
+                uint8_t* stg = smem + (half == 0 ? C::kOffQ : C::kOffDO) + s * C::kTileBytes;
+#pragma unroll
+                for (int k16 = 0; k16 < D / 32; ++k16) {  // 16 columns: half a box row
+                    uint32_t v[16];
+                    bwd_tmem_ld16(tDQ + static_cast<uint32_t>(half * (D / 2) + 16 * k16), v);
+                    bwd_tmem_ld_wait16(v);
+                    uint8_t* rowp = stg + (k16 / 2) * C::kAtomBytes + t * 128;
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int ch = (k16 % 2) * 4 + c4;
+                        *reinterpret_cast<uint4*>(rowp + ((ch ^ (t & 7)) << 4)) =
+                            make_uint4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+                    }
+                }
+                if (half == 0) tc_fence_before();  // every load of dQ(j) precedes DQFree
+                fence_proxy_async_smem();          // the staged rows are read by the TMA reductions
+                __syncwarp();
+                if (lane == 0) {
+                    if (half == 0) mbar_arrive(bar(C::kBarDQFree));
+                    mbar_arrive(bar((half == 0 ? C::kBarStaged : C::kBarStagedDO) + s));
+                }
+            }
+            if (!fine) break;
+        }
     } else if (warp >= 8) {
         regs_decrease<C::kOtherRegs>();
       if (!has_work) {
@@ -361,25 +459,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // tile, warpgroup 1's in its dO tile) into the fp32 accumulator and
         // hands the stage back to the producer once the reductions have read
         // it.  The gradient warpgroups never wait for the L2.
+        // (Read-out layout: each half as soon as it is staged, the dO tile's
+        // columns [d/2, d) first.)
         if (lane == 0) {
             for (int it = 0; it < T; ++it) {
                 const int s = it % C::kStages;
-                if (!bwd_wait(bar(C::kBarStaged + s), (it / C::kStages) & 1, abort_flag, p, 39)) break;
+                const uint32_t ph = (it / C::kStages) & 1;
                 const int qt = qt_begin + it % nqt;
                 const int bh = b * p.H + kvh * p.group + it / nqt;
+                if (!kRead && !bwd_wait(bar(C::kBarStaged + s), ph, abort_flag, p, 39)) break;
+                bool got = true;
 #pragma unroll
-                for (int w = 0; w < 2; ++w) {
+                for (int i = 0; i < 2; ++i) {
+                    const int w = kRead ? 1 - i : i;  // w = 0: columns [0, d/2) in the Q tile
+                    if (kRead) {
+                        got = bwd_wait(bar((w == 0 ? C::kBarStaged : C::kBarStagedDO) + s), ph, abort_flag, p, 39);
+                        if (!got) break;
+                    }
                     const uint32_t stg = sbase + (w == 0 ? C::kOffQ : C::kOffDO) + s * C::kTileBytes;
 #pragma unroll
                     for (int h = 0; h < D / 64; ++h)
                         tma_reduce_add_3d(&map_dq, stg + h * C::kAtomBytes, w * (D / 2) + 32 * h, qt * 128, bh);
                     tma_store_commit();  // one group per half
                 }
-                bulk_wait_read<1>();  // warpgroup 0's half (in the Q tile) has been read
-                mbar_arrive(bar(C::kBarEmpty + s));
+                if (!got) break;
+                // the first-committed half has been read, then the other
+                bulk_wait_read<1>();
+                mbar_arrive(bar((kRead ? C::kBarEmptyDO : C::kBarEmpty) + s));
                 bulk_wait_read<0>();
-                mbar_arrive(bar(C::kBarEmptyDO + s));
+                mbar_arrive(bar((kRead ? C::kBarEmpty : C::kBarEmptyDO) + s));
             }
+            bulk_wait_read<0>();  // nothing may still read shared memory at the exit
         }
       } else if (warp == kBwdMmaWarp) {
         // ------------------------------------------------ tensor-core issuer
@@ -459,19 +569,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 ok = bwd_wait(bar(C::kBarDS), it & 1, abort_flag, p, 37);
                 if (!ok) break;
                 tc_fence_after();
+                auto issue_dk = [&]() {
 #pragma unroll
-                for (int kk = 0; kk < C::kRowSteps; ++kk)
-                    mma_ss<false>(tDK, kmaj(sDS, kk), mnmaj(sQ, kk), C::kIdescAcc, (it > 0 || kk > 0) ? 1u : 0u);
-                if (C::kDqOwnCols && it > 0) {  // the previous dQ has been read out
-                    ok = bwd_wait(bar(C::kBarDQFree), (it - 1) & 1, abort_flag, p, 35);
-                    if (!ok) break;
-                    tc_fence_after();
+                    for (int kk = 0; kk < C::kRowSteps; ++kk)
+                        mma_ss<false>(tDK, kmaj(sDS, kk), mnmaj(sQ, kk), C::kIdescAcc, (it > 0 || kk > 0) ? 1u : 0u);
+                };
+                auto issue_dq = [&]() {
+#pragma unroll
+                    for (int kk = 0; kk < C::kRowSteps; ++kk)
+                        mma_ss<false>(tDQ, smem_desc_sw128(sDS + kk * C::kUmmaK * 128, C::kAtomBytes, 1024),
+                                      mnmaj(sK, kk), C::kIdescDQ, kk > 0 ? 1u : 0u);
+                    tc_commit(bar(C::kBarDQ));
+                };
+                if (kRead) {
+                    // dQ first: the read-out stages its dO-tile half while dK runs
+                    issue_dq();
+                    issue_dk();
+                    tc_commit(bar(C::kBarDK));
+                } else {
+                    issue_dk();
+                    if (C::kDqOwnCols && it > 0) {  // the previous dQ has been read out
+                        ok = bwd_wait(bar(C::kBarDQFree), (it - 1) & 1, abort_flag, p, 35);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    issue_dq();
                 }
-#pragma unroll
-                for (int kk = 0; kk < C::kRowSteps; ++kk)
-                    mma_ss<false>(tDQ, smem_desc_sw128(sDS + kk * C::kUmmaK * 128, C::kAtomBytes, 1024),
-                                  mnmaj(sK, kk), C::kIdescDQ, kk > 0 ? 1u : 0u);
-                tc_commit(bar(C::kBarDQ));
                 // the next tile's scores (late order: they run during dQ's read-out)
                 if (!C::kEarlyS && it + 1 < T) {
                     ok = bwd_wait(bar(C::kBarFull + (it + 1) % C::kStages), ((it + 1) / C::kStages) & 1,
@@ -498,7 +621,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t lane_off = static_cast<uint32_t>(wi * 32) << 16;
         const uint32_t tS = tmem + lane_off + C::kColS + 64u * static_cast<uint32_t>(w);
         const uint32_t tDP = tmem + lane_off + C::kColDP + 64u * static_cast<uint32_t>(w);
-        const uint32_t tDQ = tmem + lane_off + C::kColDQ + static_cast<uint32_t>(w * (D / 2));
+        [[maybe_unused]] const uint32_t tDQ = tmem + lane_off + C::kColDQ + static_cast<uint32_t>(w * (D / 2));
         const long long key = static_cast<long long>(kb) * 128 + t;
         const bool key_valid = key < p.Nkv;  // rows past Nkv were zero-filled: weight 0
         const float c = p.scale_log2;
@@ -565,8 +688,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (T > 0) ok = p_phase(0);
         for (int it = 0; ok && it < T; ++it) {
             const int s = it % C::kStages;
-            const int qt = qt_begin + it % nqt;
-            const int bh = b * p.H + kvh * p.group + it / nqt;
 
             // dS^T = P^T o (dP^T - D), as 16-bit pairs into row t of atom w of
             // the dS tile (free: the previous dK and dQ have completed)
@@ -607,34 +728,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 if (!ok) break;
             }
 
-            // this tile's dQ (query row t, columns [w d/2, (w+1) d/2)): staged as
-            // fp32 boxes of 32 columns (128-byte swizzle) in the stage's Q tile
-            // (w = 0) or dO tile (w = 1), which the reducer adds into the
-            // accumulator
-            got = bwd_wait(bar(C::kBarDQ), it & 1, abort_flag, p, 43);
-            ok = __all_sync(0xffffffffu, got);
-            if (!ok) break;
-            tc_fence_after();
-            uint8_t* stg = smem + (w == 0 ? C::kOffQ : C::kOffDO) + s * C::kTileBytes;
-            uint32_t v[D / 64][32];
+            if constexpr (!kRead) {
+                // (384-thread layout) this tile's dQ (query row t, columns
+                // [w d/2, (w+1) d/2)): staged as fp32 boxes of 32 columns
+                // (128-byte swizzle) in the stage's Q tile (w = 0) or dO tile
+                // (w = 1), which the reducer adds into the accumulator
+                got = bwd_wait(bar(C::kBarDQ), it & 1, abort_flag, p, 43);
+                ok = __all_sync(0xffffffffu, got);
+                if (!ok) break;
+                tc_fence_after();
+                uint8_t* stg = smem + (w == 0 ? C::kOffQ : C::kOffDO) + s * C::kTileBytes;
+                uint32_t v[D / 64][32];
 #pragma unroll
-            for (int h = 0; h < D / 64; ++h) tmem_ld32(tDQ + 32u * h, v[h]);
+                for (int h = 0; h < D / 64; ++h) tmem_ld32(tDQ + 32u * h, v[h]);
 #pragma unroll
-            for (int h = 0; h < D / 64; ++h) tmem_ld_wait(v[h]);
+                for (int h = 0; h < D / 64; ++h) tmem_ld_wait(v[h]);
 #pragma unroll
-            for (int h = 0; h < D / 64; ++h) {
-                uint8_t* rowp = stg + h * C::kAtomBytes + t * 128;
+                for (int h = 0; h < D / 64; ++h) {
+                    uint8_t* rowp = stg + h * C::kAtomBytes + t * 128;
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                    *reinterpret_cast<uint4*>(rowp + ((ch ^ (t & 7)) << 4)) =
-                        make_uint4(v[h][4 * ch], v[h][4 * ch + 1], v[h][4 * ch + 2], v[h][4 * ch + 3]);
-            }
-            tc_fence_before();
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bar(C::kBarDQFree));    // its tensor-memory columns are free
-                mbar_arrive(bar(C::kBarStaged + s));  // the reducer may read the staged rows
+                    for (int ch = 0; ch < 8; ++ch)
+                        *reinterpret_cast<uint4*>(rowp + ((ch ^ (t & 7)) << 4)) =
+                            make_uint4(v[h][4 * ch], v[h][4 * ch + 1], v[h][4 * ch + 2], v[h][4 * ch + 3]);
+                }
+                tc_fence_before();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(C::kBarDQFree));    // its tensor-memory columns are free
+                    mbar_arrive(bar(C::kBarStaged + s));  // the reducer may read the staged rows
+                }
             }
             // the next tile's P^T (late order)
             if (!C::kEarlyS && it + 1 < T) {
@@ -707,18 +830,18 @@ cudaError_t launch_bwd_variant(const CUtensorMap& q, const CUtensorMap& k, const
                                const CUtensorMap& dout, const CUtensorMap& dk, const CUtensorMap& dv,
                                const CUtensorMap& dq, const BwdParams& p, unsigned int grid,
                                cudaStream_t stream) {
-    using C = BwdCfg<D, F16>;
+    using C = BwdCfg<D, F16, bwd_read_layout<D, kCausal>()>;
     auto kern = fa_bwd_kernel<D, F16, kCausal>;
     // The register split relies on the compiled kernel holding exactly
-    // kBwdLaunchRegs per thread (a setmaxnreg.inc without the registers behind
+    // C::kLaunchRegs per thread (a setmaxnreg.inc without the registers behind
     // it would never return); refuse to launch otherwise.
     cudaFuncAttributes attr;
     cudaError_t e = cudaFuncGetAttributes(&attr, kern);
     if (e != cudaSuccess) return e;
-    if (attr.numRegs != static_cast<int>(kBwdLaunchRegs)) return cudaErrorInvalidConfiguration;
+    if (attr.numRegs != static_cast<int>(C::kLaunchRegs)) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemBytes));
     if (e != cudaSuccess) return e;
-    kern<<<grid, kBwdThreads, C::kSmemBytes, stream>>>(q, k, v, dout, dk, dv, dq, p);
+    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(q, k, v, dout, dk, dv, dq, p);
     return cudaGetLastError();
 }
 
