@@ -77,7 +77,8 @@ void bwd_tensor_bytes(int64_t B, int64_t H, int64_t H_kv, int64_t N_q, int64_t N
 cudaError_t launch_bwd_prep(const BwdPrepParams& p, int d, int dtype, cudaStream_t stream);
 cudaError_t launch_bwd_dq(const BwdDqParams& p, int dtype, cudaStream_t stream);
 
-// Main kernel: grid = B * H_kv * n_kv_blocks CTAs of 384 threads.  Maps:
+// Main kernel: grid = B * H_kv * n_kv_blocks CTAs of 384 threads (512 for
+// d = 128 without the causal mask).  Maps:
 // q, dO over [B*H, Nq, d]; k, v, dk, dv over [B*H_kv, Nkv, d] (input dtype);
 // dq over the fp32 accumulator [B*H, Nq, d].
 cudaError_t launch_bwd_bf16(int d, const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
