@@ -245,7 +245,99 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi every 100 ms"}
+
+
+class NvmlClockSampler(ClockSampler):
+    """The same record from NVML in-process (the driver's libnvidia-ml, read
+    only): SM clock, its maximum and the clock event reasons every 2 ms, so
+    that a timed region of a few tens of milliseconds (a short graph) still
+    holds tens of samples where nvidia-smi's 100 ms cadence gives one.
+    `open` returns None where NVML is unavailable; nvidia-smi is then used."""
+    REASON_BITS = ((0x8, "hw_slowdown"), (0x40, "hw_thermal_slowdown"), (0x20, "sw_thermal_slowdown"),
+                   (0x4, "sw_power_cap"))
+    INTERVAL_S = 0.002
+
+    @classmethod
+    def open(cls, gpu_index: int):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return None
+        except (OSError, AttributeError):
+            return None
+        handle = ctypes.c_void_p()
+        found = False
+        try:  # the CUDA device's NVML handle, through its PCI address
+            import torch
+            pr = torch.cuda.get_device_properties(gpu_index)
+            bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+            found = lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(handle)) == 0
+        except Exception:  # noqa: BLE001 - fall back to the index
+            found = False
+        if not found and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index), ctypes.byref(handle)) != 0:
+            return None
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+        if reasons is None:
+            return None
+        smp = cls(gpu_index)
+        smp.lib, smp.handle, smp.reasons_fn = lib, handle, reasons
+        return smp
+
+    def _sample(self):
+        import ctypes
+        clk, mx, rs = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        if (self.lib.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) != 0 or
+                self.lib.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) != 0 or
+                self.reasons_fn(self.handle, ctypes.byref(rs)) != 0):
+            return None
+        return (clk.value, mx.value, rs.value)
+
+    def _run(self):
+        while not self._stop.is_set():
+            r = self._sample()
+            if r is not None:
+                self.rows.append(r)
+            self._stop.wait(self.INTERVAL_S)
+
+    def __enter__(self):
+        import threading
+        self.rows = []
+        self._stop = threading.Event()
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+        t0 = time.time()
+        while not self.rows and time.time() - t0 < 1.0:
+            time.sleep(0.001)
+        self.start_rows = len(self.rows)
+        return self
+
+    def count(self) -> int:
+        return len(self.rows)
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        self._thread.join(timeout=2.0)
+        return False
+
+    def summary(self, busy_threshold_frac: float = 0.0):
+        rows = self.rows[min(self.start_rows, max(0, len(self.rows) - 1)):]
+        try:
+            self.lib.nvmlShutdown()
+        except Exception:  # noqa: BLE001
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({name for _, _, bits in rows for bit, name in self.REASON_BITS if bits & bit})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "source": "NVML every 2 ms"}
+
+
+def clock_sampler(gpu_index: int):
+    """NVML in-process where it loads, else nvidia-smi."""
+    return NvmlClockSampler.open(gpu_index) or ClockSampler(gpu_index)
 
 
 # --------------------------------------------------------------- CPU oracle
@@ -557,7 +649,7 @@ def run_ours(args, w):
     torch.cuda.synchronize(dev)
     launches = 0
     step_events = []
-    with ClockSampler(local) as clocks:
+    with clock_sampler(local) as clocks:
         with torch.cuda.stream(stream):
             if flush:
                 for _ in range(args.steps):
@@ -709,7 +801,7 @@ def run_ours(args, w):
         e2e={"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
              "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
         gpu_launches=timed_launches,
-        clocks=dict({k2: clk[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
+        clocks=dict({k2: clk[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "source") if k2 in clk},
                     window=clock_window),
         entry=entry_name)
     if world == 1 and not args.no_cpu_baseline:

@@ -68,6 +68,16 @@ def test_short_queries():
     check(1, 4, 4, 7, 900, 64, "f16", True, seed=641)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_multi_head_sweep_d128(dtype):
+    """d = 128 without the causal mask (the kernel with the dQ read-out
+    warpgroup): two query heads per key/value head, four query tiles each
+    with a ragged last one, so one CTA sweeps eight tiles through its
+    two-stage ring, changes query head half way, and stages and reduces dQ
+    of partial tiles."""
+    check(1, 4, 2, 390, 256, 128, dtype, False, seed=660)
+
+
 def test_long_keys_one_head():
     check(1, 1, 1, 64, 2000, 128, "bf16", False, seed=650)
 
