@@ -834,6 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const bool skip = *abort_flag != 0u;
+
     if (skip) {
         // nothing issued: go straight to the teardown
     } else if (warp >= 8) {
@@ -843,6 +844,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // no visible key: nothing to load or multiply
       } else if (warp == kLoadWarp) {
         // ------------------------------------------------------ TMA producer
+        // a launch that follows in the stream with programmatic serialization
+        // (the split last wave) may place its CTAs as this grid's leave the SMs
+        if (lane == 0) asm volatile("griddepcontrol.launch_dependents;");
         if (!TF32 && pack) zero_unloaded_q<C::kTileBytes, C::kAtoms, C::kAtomBytes>(smem + C::kOffQ, pack_rows, lane);
         if constexpr (TF32) {
             produce_tf32<D>(map_q, map_k, map_v, p, smem, sbase, lane, row0, bh, kvh, t_begin, T, abort_flag);
@@ -1383,6 +1387,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    // launched with programmatic serialization (the split last wave): this
+    // CTA completes only after the grid before it in the stream, so that
+    // work after this launch still sees both (returns at once otherwise)
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;");
 }
 
 template <bool TF32, int D, bool F16, bool kCausal, bool kOneTile>
@@ -1411,13 +1419,21 @@ cudaError_t launch_fwd_variant(const CUtensorMap& q, const CUtensorMap& k, const
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = C::kSmemBytes;
         cfg.stream = stream;
-        cudaLaunchAttribute attr_cluster[1];
+        cudaLaunchAttribute attr_cluster[2];
         attr_cluster[0].id = cudaLaunchAttributeClusterDimension;
         attr_cluster[0].val.clusterDim.x = static_cast<unsigned>(p.splits);
         attr_cluster[0].val.clusterDim.y = 1;
         attr_cluster[0].val.clusterDim.z = 1;
         cfg.attrs = attr_cluster;
         cfg.numAttrs = 1;
+        // the last wave of an automatic plan (item_offset > 0) follows the
+        // full waves' launch and shares no data with it: its CTAs may start
+        // as that launch's CTAs finish
+        if (p.item_offset > 0) {
+            attr_cluster[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr_cluster[1].val.programmaticStreamSerializationAllowed = 1;
+            cfg.numAttrs = 2;
+        }
         e = cudaLaunchKernelEx(&cfg, kern, q, k, v, o, p);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
