@@ -207,3 +207,48 @@ def test_automatic_partitions(B, H, H_kv, N, d, dtype):
     assert np.isfinite(o).all() and np.isfinite(lse).all()
     err_o, err_l = compare_ex(dtype, o, lse, q, k, v)
     assert err_o <= tol_o_dtype(dtype) and err_l <= TOL_LSE, (err_o, err_l)
+
+
+@pytest.mark.parametrize("B,H,N,d", [(2, 32, 2048, 128), (4, 16, 2048, 64)])
+def test_dependent_last_wave_in_a_chain(B, H, N, d):
+    """Where the plan runs its last wave as a second launch that may start
+    while the full waves are still running, a later call on the same stream
+    still sees the whole output: three calls chained through O (each call's
+    output is the next call's queries) give the same bits with and without a
+    synchronize between the calls, and the first step matches the oracle."""
+    bf16 = fab.FA_DTYPE_BF16
+    if fab.fa_fwd_launches(B, H, N, d, bf16) != 2:
+        pytest.skip("the plan on this device has no split last wave for this shape")
+    w = I.custom(B, H, N, d, "bf16", seed=1201 + d)
+    q, k, v = I.make(w)
+    from .gpu_util import compare, to_device
+    tq, tk, tv = (to_device(x, "bf16") for x in (q, k, v))
+    s = torch.cuda.current_stream()
+
+    def chain(sync):
+        outs, x = [], tq
+        for _ in range(3):
+            o = torch.full_like(tq, float("nan"))
+            lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+            st = fab.fa_fwd(x.data_ptr(), tk.data_ptr(), tv.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                            B, H, N, d, float(w.scale), bf16, s.cuda_stream)
+            assert st == fab.FA_OK, (st, fab.fa_last_error_message())
+            if sync:
+                torch.cuda.synchronize()
+            outs.append((o, lse))
+            x = o
+        torch.cuda.synchronize()
+        assert fab.fa_device_status(s.cuda_stream) == fab.FA_OK
+        return outs
+
+    ref = chain(True)
+    for _ in range(3):
+        got = chain(False)
+        for (o_r, l_r), (o_g, l_g) in zip(ref, got):
+            assert torch.equal(o_r.view(torch.int16), o_g.view(torch.int16))
+            assert torch.equal(l_r, l_g)
+    o1, l1 = ref[0]
+    last_head = np.stack([np.full(64, B - 1), np.full(64, H - 1), np.linspace(0, N - 1, 64).astype(np.int64)], 1)
+    rows = np.concatenate([I.sample_rows(w, 192), last_head])   # the last head lies in the split last wave
+    err_o, err_l = compare(w, o1.float().cpu().numpy(), l1.cpu().numpy(), q, k, v, rows=rows)
+    assert err_o <= tol_o_dtype("bf16") and err_l <= TOL_LSE, (err_o, err_l)
