@@ -133,6 +133,15 @@ struct FwdCfg {
     // (measured at d = 64: early scores alone +4 %, and without turns
     // +24 % on top).
     static constexpr bool kTakeTurns = !kEarlyS;
+    // With early scores the two tiles run in step, and each softmax
+    // warpgroup waits on the release barriers of the K and V stages (both
+    // tiles' products) instead of completion barriers of its own tile: two
+    // tcgen05.commit fewer per tile and issuer, each of which costs the
+    // tensor pipe time (measured: two extra commits per tile and issuer
+    // cost 5 %; this saves 5 % at d = 64.  Release barriers per tile,
+    // waited for by their own tile's softmax, measured 4 % slower at
+    // d = 128 and gained less at d = 64.)
+    static constexpr bool kStageDone = kEarlyS;
     // row maxima from the reducing TMEM load (see the softmax loop)
     static constexpr bool kHwMax = D == 64;
 
@@ -155,7 +164,7 @@ struct FwdCfg {
     static constexpr int kBarKEmpty = kBarKFull + kKStages;
     static constexpr int kBarVFull = kBarKEmpty + kKStages;
     static constexpr int kBarVEmpty = kBarVFull + kVStages;
-    static constexpr int kBarSFull = kBarVEmpty + kVStages;  // [2]
+    static constexpr int kBarSFull = kBarVEmpty + kVStages;  // [2] (not kStageDone)
     static constexpr int kBarPFull = kBarSFull + 2;          // [2 tiles][2 halves]
     static constexpr int kBarOFull = kBarPFull + 4;          // [2]
     static constexpr int kBarEpi = kBarOFull + 2;            // [2]
@@ -165,7 +174,7 @@ struct FwdCfg {
     static constexpr int kBarVRaw = kBarKRaw + kKStages;
     static constexpr int kBarTurn = kBarVRaw + 1;  // [2]: softmax warpgroup w may start a tile
     static constexpr int kBarSFree = kBarTurn + 2;   // [2] kEarlyS: S_w read (4 warps)
-    static constexpr int kBarPVDone = kBarSFree + 2; // [2] kEarlyS: O_w += P_w V done
+    static constexpr int kBarPVDone = kBarSFree + 2; // [2] kEarlyS, not kStageDone: O_w += P_w V done
     static constexpr int kBarVRawFree = kBarPVDone + 2;  // fp32 only: the raw V buffer was transposed
     static constexpr int kBarMerge = kBarVRawFree + 1;    // in-cluster merge: the peers' rows landed
     static constexpr int kNumBars = kBarMerge + 1;
@@ -960,7 +969,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) {
                 tc_fence_after();
                 issue_qk(0);
-                tc_commit(bar(C::kBarSFull + w));
+                if (!C::kStageDone) tc_commit(bar(C::kBarSFull + w));
                 tc_commit(bar(C::kBarKEmpty + 0));
             }
             for (int j = 0; ok && j < T; ++j) {
@@ -974,7 +983,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     tc_fence_after();
                     issue_qk(ks);
-                    tc_commit(bar(C::kBarSFull + w));
+                    if (!C::kStageDone) tc_commit(bar(C::kBarSFull + w));
                     tc_commit(bar(C::kBarKEmpty + ks));
                 }
                 ok = wait_phase(bar(C::kBarVFull + vs), (j / C::kVStages) & 1, abort_flag, p, 5);
@@ -991,7 +1000,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_pv(vs, true, C::kPvSteps / 2, C::kPvSteps);
                 tc_commit(bar(C::kBarVEmpty + vs));
                 if (C::kEarlyS) {
-                    tc_commit(bar(C::kBarPVDone + w));
+                    if (!C::kStageDone) tc_commit(bar(C::kBarPVDone + w));
                     if (j + 1 == T) tc_commit(bar(C::kBarOFull + w));
                 } else if (j + 1 < T) {
                     ok = wait_phase(bar(C::kBarKFull + ks), ((j + 1) / C::kKStages) & 1, abort_flag, p, 7);
@@ -1090,7 +1099,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!kFlagTurns && take_turns && w == 1 && lane == 0) mbar_arrive(bar(C::kBarTurn + 0));
         const int T_rows = active ? T : 0;
         for (int j = 0; j < T_rows; ++j) {  // T <= 0: no key tile
-            bool got = wait_phase(bar(C::kBarSFull + w), j & 1, abort_flag, p, 10);
+            // S_w(j) computed (kStageDone: both tiles' scores, which release K stage j)
+            bool got = C::kStageDone ? wait_phase(bar(C::kBarKEmpty + j % C::kKStages), (j / C::kKStages) & 1,
+                                                  abort_flag, p, 10)
+                                     : wait_phase(bar(C::kBarSFull + w), j & 1, abort_flag, p, 10);
             ok = __all_sync(0xffffffffu, got);
             if (!ok) break;
             if (take_turns) {
@@ -1134,7 +1146,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (that product is not ordered before this tile's scores)
             auto wait_prev_product = [&]() -> bool {
                 if (!C::kEarlyS || j == 0) return true;
-                return __all_sync(0xffffffffu, wait_phase(bar(C::kBarPVDone + w), (j - 1) & 1, abort_flag, p, 15));
+                // (kStageDone: both tiles' products, which release V stage j-1)
+                const bool done = C::kStageDone ? wait_phase(bar(C::kBarVEmpty + (j - 1) % C::kVStages),
+                                                             ((j - 1) / C::kVStages) & 1, abort_flag, p, 15)
+                                                : wait_phase(bar(C::kBarPVDone + w), (j - 1) & 1, abort_flag, p, 15);
+                return __all_sync(0xffffffffu, done);
             };
 
             // keys of this tile visible to this row (<= 0: none, >= 128: all);
